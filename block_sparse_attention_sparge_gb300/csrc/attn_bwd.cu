@@ -1,0 +1,636 @@
+// Block-sparse attention backward on sm_103a (tcgen05 + TMEM + TMA).
+//
+// Method: "SpargeAttention2: Trainable Sparse Attention via Hybrid Top-k+Top-p
+// Masking and Distillation Fine-Tuning", section "Abstract" (the sparse
+// attention is trainable), and the mindverse page "Optimierung der Effizienz
+// von Video-Diffusionsmodellen durch SpargeAttention2", section "Effiziente
+// Kernel-Implementierung und Modellanpassung" (forward and backward skip the
+// masked tiles).  The mask is a constant; per kept (q-block i, kv-block j):
+//   P = exp(scale*Q_i K_j^T - LSE_i),  dP = dO_i V_j^T,  dS = P * (dP - D_i)
+//   dV_j += P^T dO_i,  dK_j += scale * dS^T Q_i,  dQ_i += scale * dS K_j
+// with D_t = sum_c dO_tc O_tc.
+//
+// Three kernels, no atomics (deterministic):
+//   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads).
+//   bwd_dkdv_kernel   one CTA per kv-block, loops over the q-blocks that keep
+//                     it (CSC list).  S and dP are recomputed into TMEM
+//                     (M = 128 query rows); dV^T and dK^T accumulate in TMEM
+//                     as M = d tiles, dV^T += dO^T P and dK^T += Q^T dS, with
+//                     dO, Q, P and dS read in the MN-major smem layout.
+//   bwd_dq_kernel     one CTA per q-block, loops over its kept kv-blocks (CSR
+//                     list); recomputes S, dP and dS and accumulates
+//                     dQ += dS K in TMEM.
+// Roles per CTA: warps 0-3 compute (thread r = TMEM lane r), warp 4 TMA
+// producer, warp 5 MMA issuer.  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sparge {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 64;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- D = rowsum(dO * O)
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        long long rows, float* __restrict__ delta) {
+  constexpr int CH = D / 8;        // 16-byte chunks per row
+  constexpr int RPB = 256 / CH;    // rows per block pass
+  const long long r = (long long)blockIdx.x * RPB + threadIdx.x / CH;
+  const int c = threadIdx.x % CH;
+  float s = 0.f;
+  if (r < rows) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + r * D) + c);
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + r * D) + c);
+    const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = __bfloat1622float2(ha[e]);
+      const float2 fb = __bfloat1622float2(hb[e]);
+      s = fmaf(fa.x, fb.x, s);
+      s = fmaf(fa.y, fb.y, s);
+    }
+  }
+#pragma unroll
+  for (int off = CH / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (c == 0 && r < rows) delta[r] = s;
+}
+
+// Loads 64 fp32 columns of one TMEM lane (4 x 16) starting at `addr`.
+__device__ __forceinline__ void tmem_ld64(uint32_t addr, float (&x)[64]) {
+  uint32_t ra[16], rb[16], rc[16], rd[16];
+  SPARGE_TMEM_LD_X16(addr + 0, ra);
+  SPARGE_TMEM_LD_X16(addr + 16, rb);
+  SPARGE_TMEM_LD_X16(addr + 32, rc);
+  SPARGE_TMEM_LD_X16(addr + 48, rd);
+  SPARGE_TMEM_WAIT_LD16(ra);
+  SPARGE_TMEM_WAIT_LD16(rb);
+  SPARGE_TMEM_WAIT_LD16(rc);
+  SPARGE_TMEM_WAIT_LD16(rd);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    x[c] = __uint_as_float(ra[c]);
+    x[16 + c] = __uint_as_float(rb[c]);
+    x[32 + c] = __uint_as_float(rc[c]);
+    x[48 + c] = __uint_as_float(rd[c]);
+  }
+}
+
+// Writes 64 bf16 values (one 128-byte row) into a 128-byte-swizzled tile.
+__device__ __forceinline__ void store_row_sw128(uint8_t* tile, int row, const uint32_t (&pk)[32]) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4 v;
+    v.x = pk[4 * ch + 0];
+    v.y = pk[4 * ch + 1];
+    v.z = pk[4 * ch + 2];
+    v.w = pk[4 * ch + 3];
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, ch * 16)) = v;
+  }
+}
+
+// ---------------------------------------------------------------- dK, dV
+template <int D>
+struct DkdvCfg {
+  static constexpr int NST = 2;
+  static constexpr int KCH = D / 64;
+  static constexpr uint32_t kKV = kBN * D * 2;  // one K or V tile
+  static constexpr uint32_t kQ = kBM * D * 2;   // one Q or dO tile
+  static constexpr uint32_t kP = kBM * kBN * 2;
+  static constexpr uint32_t off_k = 0;
+  static constexpr uint32_t off_v = off_k + kKV;
+  static constexpr uint32_t off_q = off_v + kKV;                 // NST stages of Q
+  static constexpr uint32_t off_do = off_q + NST * kQ;           // NST stages of dO
+  static constexpr uint32_t off_p = off_do + NST * kQ;
+  static constexpr uint32_t off_ds = off_p + kP;
+  static constexpr uint32_t off_bar = off_ds + kP;
+  static constexpr int B_KV = 0;
+  static constexpr int B_QF = 1;
+  static constexpr int B_QE = B_QF + NST;
+  static constexpr int B_SF = B_QE + NST;  // 2
+  static constexpr int B_PSF = B_SF + 2;   // count 128
+  static constexpr int B_PSE = B_PSF + 1;
+  static constexpr int B_DONE = B_PSE + 1;
+  static constexpr int NBAR = B_DONE + 1;
+  static constexpr uint32_t off_slot = off_bar + NBAR * 8;
+  static constexpr uint32_t bytes = off_slot + 16;
+  static constexpr uint32_t smem_alloc = bytes + 1024;
+  static constexpr uint32_t tmem_cols = 512;  // S/dP x2 [0,256), dV^T [256,320), dK^T [320,384)
+  static constexpr uint32_t col_dv = 256;
+  static constexpr uint32_t col_dk = 320;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const float* __restrict__ lse, const float* __restrict__ delta,
+                    const int32_t* __restrict__ col_idx, const int32_t* __restrict__ col_cnt, int N,
+                    int Mq, int Mk, float scale, float scale_log2, __nv_bfloat16* __restrict__ dk,
+                    __nv_bfloat16* __restrict__ dv, int32_t* __restrict__ status) {
+  using C = DkdvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t s0 = smem_u32(sm);
+  auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / Mk;
+  const int j = blockIdx.x % Mk;
+  const long long col_id = (long long)bh * Mk + j;
+  const int n = min(max(__ldg(col_cnt + col_id), 0), Mq);
+  const int32_t* list = col_idx + col_id * Mq;
+  const int kv_valid = min(kBN, N - j * kBN);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) mbar_init(bar(i), i == C::B_PSF ? 128u : 1u);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(slot), C::tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+
+  if (warp == 4) {
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::kKV);
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_3d(s0 + C::off_k + c * kBN * 128, &tmK, bar(C::B_KV), c * 64, j * kBN, bh);
+        tma_load_3d(s0 + C::off_v + c * kBN * 128, &tmV, bar(C::B_KV), c * 64, j * kBN, bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < n; ++t) {
+        const int s = t % C::NST;
+        if (t >= C::NST && !mbar_wait(bar(C::B_QE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+          report_error(status, SPARGE_ERR_TIMEOUT);
+          break;
+        }
+        const int i = min(max(__ldg(list + t), 0), Mq - 1);
+        mbar_arrive_expect_tx(bar(C::B_QF + s), 2 * C::kQ);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_3d(s0 + C::off_q + s * C::kQ + c * kBM * 128, &tmQ, bar(C::B_QF + s), c * 64,
+                      i * kBM, bh);
+          tma_load_3d(s0 + C::off_do + s * C::kQ + c * kBM * 128, &tmDO, bar(C::B_QF + s), c * 64,
+                      i * kBM, bh);
+        }
+        issued = t + 1;
+      }
+      for (int t = max(0, issued - C::NST); t < issued; ++t)
+        mbar_wait(bar(C::B_QF + t % C::NST), (t / C::NST) & 1, kWaitTimeoutNs);
+    }
+  } else if (warp == 5) {
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);   // [q x kv], K = d
+      constexpr uint32_t idG = idesc_bf16(kBM, kBN, true, true);     // [d x kv], K = q
+      bool ok = mbar_wait(bar(C::B_KV), 0, kWaitTimeoutNs);
+      for (int t = 0; ok && t <= n; ++t) {
+        if (t < n) {
+          const int s = t % C::NST;
+          if (!mbar_wait(bar(C::B_QF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qb = s0 + C::off_q + s * C::kQ;
+          const uint32_t ob = s0 + C::off_do + s * C::kQ;
+          const uint32_t dS = tmem + (t & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+            const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+            tc_mma_bf16(dS, sdesc_sw128(qb + ko, 16, 1024),
+                        sdesc_sw128(s0 + C::off_k + kko, 16, 1024), idS, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+            const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+            tc_mma_bf16(dS + 64, sdesc_sw128(ob + ko, 16, 1024),
+                        sdesc_sw128(s0 + C::off_v + kko, 16, 1024), idS, kk > 0);
+          }
+          tc_commit(bar(C::B_SF + (t & 1)));
+        }
+        if (t >= 1) {
+          const int u = t - 1;
+          const int su = u % C::NST;
+          if (!mbar_wait(bar(C::B_PSF), u & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qb = s0 + C::off_q + su * C::kQ;
+          const uint32_t ob = s0 + C::off_do + su * C::kQ;
+#pragma unroll
+          for (int kk = 0; kk < kBM / 16; ++kk) {
+            // A = dO^T (M = d, MN-major: 64-element chunks kBM*128 apart),
+            // B = P (N = kv, MN-major); K = 16 query rows per step.
+            tc_mma_bf16(tmem + C::col_dv, sdesc_sw128(ob + kk * 2048, kBM * 128, 1024),
+                        sdesc_sw128(s0 + C::off_p + kk * 2048, kBM * 128, 1024), idG,
+                        (u > 0 || kk > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kBM / 16; ++kk) {
+            tc_mma_bf16(tmem + C::col_dk, sdesc_sw128(qb + kk * 2048, kBM * 128, 1024),
+                        sdesc_sw128(s0 + C::off_ds + kk * 2048, kBM * 128, 1024), idG,
+                        (u > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_QE + su));
+          tc_commit(bar(C::B_PSE));
+        }
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+      tc_commit(bar(C::B_DONE));
+      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+    }
+  } else {
+    const int r = threadIdx.x;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const int i = min(max(__ldg(list + t), 0), Mq - 1);
+      const int row = i * kBM + r;
+      const bool rv = row < N;
+      const float lse2 = rv ? __ldg(lse + (long long)bh * N + row) * kLog2e : 0.f;
+      const float drow = rv ? __ldg(delta + (long long)bh * N + row) : 0.f;
+      if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t pk[32], dk_[32];
+      {
+        float s[64], dp[64];
+        tmem_ld64(lane_base + (t & 1) * 128, s);
+        tmem_ld64(lane_base + (t & 1) * 128 + 64, dp);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float p0 = exp2f(fmaf(s[c], scale_log2, -lse2));
+          float p1 = exp2f(fmaf(s[c + 1], scale_log2, -lse2));
+          if (!rv || c >= kv_valid) p0 = 0.f;
+          if (!rv || c + 1 >= kv_valid) p1 = 0.f;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+          dk_[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
+        }
+      }
+      if (t >= 1 && !warp_wait(bar(C::B_PSE), (t - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      store_row_sw128(sm + C::off_p, r, pk);
+      store_row_sw128(sm + C::off_ds, r, dk_);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PSF));
+    }
+    if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+    // Epilogue: thread r holds column r of dV^T / dK^T (= feature r of 64 kv rows).
+    bool have = ok && n > 0;
+    if (have) {
+      have = warp_wait(bar(C::B_PSE), (n - 1) & 1);
+      if (!have) report_error(status, SPARGE_ERR_TIMEOUT);
+    }
+    tc_fence_after();
+    const long long base = ((long long)bh * N + (long long)j * kBN) * D + r;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBN; c0 += 16) {
+      uint32_t rv_[16], rk_[16];
+      if (have) {
+        SPARGE_TMEM_LD_X16(lane_base + C::col_dv + c0, rv_);
+        SPARGE_TMEM_LD_X16(lane_base + C::col_dk + c0, rk_);
+        SPARGE_TMEM_WAIT_LD16(rv_);
+        SPARGE_TMEM_WAIT_LD16(rk_);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) rv_[c] = rk_[c] = 0u;
+      }
+      if (r < D) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c0 + c < kv_valid) {
+            dv[base + (long long)(c0 + c) * D] = __float2bfloat16_rn(__uint_as_float(rv_[c]));
+            dk[base + (long long)(c0 + c) * D] =
+                __float2bfloat16_rn(__uint_as_float(rk_[c]) * scale);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------- dQ
+template <int D>
+struct DqCfg {
+  static constexpr int NST = 3;
+  static constexpr int KCH = D / 64;
+  static constexpr uint32_t kKV = kBN * D * 2;
+  static constexpr uint32_t kQ = kBM * D * 2;
+  static constexpr uint32_t kP = kBM * kBN * 2;
+  static constexpr uint32_t off_q = 0;
+  static constexpr uint32_t off_do = off_q + kQ;
+  static constexpr uint32_t off_k = off_do + kQ;
+  static constexpr uint32_t off_v = off_k + NST * kKV;
+  static constexpr uint32_t off_ds = off_v + NST * kKV;  // 2 buffers
+  static constexpr uint32_t off_bar = off_ds + 2 * kP;
+  static constexpr int B_Q = 0;
+  static constexpr int B_KF = 1;
+  static constexpr int B_VF = B_KF + NST;
+  static constexpr int B_KE = B_VF + NST;
+  static constexpr int B_SF = B_KE + NST;   // 2
+  static constexpr int B_DSF = B_SF + 2;    // 2, count 128
+  static constexpr int B_DSE = B_DSF + 2;   // 2
+  static constexpr int B_DONE = B_DSE + 2;
+  static constexpr int NBAR = B_DONE + 1;
+  static constexpr uint32_t off_slot = off_bar + NBAR * 8;
+  static constexpr uint32_t bytes = off_slot + 16;
+  static constexpr uint32_t smem_alloc = bytes + 1024;
+  static constexpr uint32_t tmem_cols = 512;  // S/dP x2 [0,256), dQ [256, 256+D)
+  static constexpr uint32_t col_dq = 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const float* __restrict__ lse, const float* __restrict__ delta,
+                  const int32_t* __restrict__ row_idx, const int32_t* __restrict__ row_cnt, int N,
+                  int Mq, int Mk, float scale, float scale_log2, __nv_bfloat16* __restrict__ dq,
+                  int32_t* __restrict__ status) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t s0 = smem_u32(sm);
+  auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / Mq;
+  const int qb = blockIdx.x % Mq;
+  const long long row_id = (long long)bh * Mq + qb;
+  const int n = min(max(__ldg(row_cnt + row_id), 0), Mk);
+  const int32_t* list = row_idx + row_id * Mk;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i)
+      mbar_init(bar(i), (i == C::B_DSF || i == C::B_DSF + 1) ? 128u : 1u);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(slot), C::tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+
+  if (warp == 4) {
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::kQ);
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_3d(s0 + C::off_q + c * kBM * 128, &tmQ, bar(C::B_Q), c * 64, qb * kBM, bh);
+        tma_load_3d(s0 + C::off_do + c * kBM * 128, &tmDO, bar(C::B_Q), c * 64, qb * kBM, bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < n; ++t) {
+        const int s = t % C::NST;
+        if (t >= C::NST && !mbar_wait(bar(C::B_KE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+          report_error(status, SPARGE_ERR_TIMEOUT);
+          break;
+        }
+        const int jj = min(max(__ldg(list + t), 0), Mk - 1);
+        mbar_arrive_expect_tx(bar(C::B_KF + s), C::kKV);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(s0 + C::off_k + s * C::kKV + c * kBN * 128, &tmK, bar(C::B_KF + s), c * 64,
+                      jj * kBN, bh);
+        mbar_arrive_expect_tx(bar(C::B_VF + s), C::kKV);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(s0 + C::off_v + s * C::kKV + c * kBN * 128, &tmV, bar(C::B_VF + s), c * 64,
+                      jj * kBN, bh);
+        issued = t + 1;
+      }
+      for (int t = max(0, issued - C::NST); t < issued; ++t) {
+        mbar_wait(bar(C::B_KF + t % C::NST), (t / C::NST) & 1, kWaitTimeoutNs);
+        mbar_wait(bar(C::B_VF + t % C::NST), (t / C::NST) & 1, kWaitTimeoutNs);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t idQ = idesc_bf16(kBM, D, false, true);
+      bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
+      for (int t = 0; ok && t <= n; ++t) {
+        if (t < n) {
+          const int s = t % C::NST;
+          const uint32_t dS = tmem + (t & 1) * 128;
+          if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+            const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+            tc_mma_bf16(dS, sdesc_sw128(s0 + C::off_q + ko, 16, 1024),
+                        sdesc_sw128(s0 + C::off_k + s * C::kKV + kko, 16, 1024), idS, kk > 0);
+          }
+          if (!mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+            const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+            tc_mma_bf16(dS + 64, sdesc_sw128(s0 + C::off_do + ko, 16, 1024),
+                        sdesc_sw128(s0 + C::off_v + s * C::kKV + kko, 16, 1024), idS, kk > 0);
+          }
+          tc_commit(bar(C::B_SF + (t & 1)));
+        }
+        if (t >= 1) {
+          const int u = t - 1;
+          const int su = u % C::NST;
+          if (!mbar_wait(bar(C::B_DSF + (u & 1)), (u >> 1) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dsb = s0 + C::off_ds + (u & 1) * C::kP;
+          const uint32_t kb = s0 + C::off_k + su * C::kKV;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            // A = dS (K-major, K = kv), B = K_j (N = d, MN-major).
+            tc_mma_bf16(tmem + C::col_dq, sdesc_sw128(dsb + kk * 32, 16, 1024),
+                        sdesc_sw128(kb + kk * 2048, kBN * 128, 1024), idQ,
+                        (u > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_KE + su));
+          tc_commit(bar(C::B_DSE + (u & 1)));
+        }
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+      tc_commit(bar(C::B_DONE));
+      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+    }
+  } else {
+    const int r = threadIdx.x;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int row = qb * kBM + r;
+    const bool rv = row < N;
+    const float lse2 = (rv && n > 0) ? __ldg(lse + (long long)bh * N + row) * kLog2e : 0.f;
+    const float drow = rv ? __ldg(delta + (long long)bh * N + row) : 0.f;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const int jj = min(max(__ldg(list + t), 0), Mk - 1);
+      const int kv_valid = N - jj * kBN;
+      if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t pk[32];
+      {
+        float s[64], dp[64];
+        tmem_ld64(lane_base + (t & 1) * 128, s);
+        tmem_ld64(lane_base + (t & 1) * 128 + 64, dp);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float p0 = exp2f(fmaf(s[c], scale_log2, -lse2));
+          float p1 = exp2f(fmaf(s[c + 1], scale_log2, -lse2));
+          if (!rv || c >= kv_valid) p0 = 0.f;
+          if (!rv || c + 1 >= kv_valid) p1 = 0.f;
+          pk[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
+        }
+      }
+      if (t >= 2 && !warp_wait(bar(C::B_DSE + (t & 1)), ((t - 2) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      store_row_sw128(sm + C::off_ds + (t & 1) * C::kP, r, pk);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DSF + (t & 1)));
+    }
+    if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+    bool have = ok && n > 0;
+    if (have) {
+      have = warp_wait(bar(C::B_DSE + ((n - 1) & 1)), ((n - 1) >> 1) & 1);
+      if (!have) report_error(status, SPARGE_ERR_TIMEOUT);
+    }
+    tc_fence_after();
+    __nv_bfloat16* qrow = dq + ((long long)bh * N + row) * D;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      uint32_t ro[16];
+      if (have) {
+        SPARGE_TMEM_LD_X16(lane_base + C::col_dq + c0, ro);
+        SPARGE_TMEM_WAIT_LD16(ro);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) ro[c] = 0u;
+      }
+      uint4 w0, w1;
+      w0.x = pack_bf16x2(__uint_as_float(ro[0]) * scale, __uint_as_float(ro[1]) * scale);
+      w0.y = pack_bf16x2(__uint_as_float(ro[2]) * scale, __uint_as_float(ro[3]) * scale);
+      w0.z = pack_bf16x2(__uint_as_float(ro[4]) * scale, __uint_as_float(ro[5]) * scale);
+      w0.w = pack_bf16x2(__uint_as_float(ro[6]) * scale, __uint_as_float(ro[7]) * scale);
+      w1.x = pack_bf16x2(__uint_as_float(ro[8]) * scale, __uint_as_float(ro[9]) * scale);
+      w1.y = pack_bf16x2(__uint_as_float(ro[10]) * scale, __uint_as_float(ro[11]) * scale);
+      w1.z = pack_bf16x2(__uint_as_float(ro[12]) * scale, __uint_as_float(ro[13]) * scale);
+      w1.w = pack_bf16x2(__uint_as_float(ro[14]) * scale, __uint_as_float(ro[15]) * scale);
+      if (rv) {
+        *reinterpret_cast<uint4*>(qrow + c0) = w0;
+        *reinterpret_cast<uint4*>(qrow + c0 + 8) = w1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::tmem_cols);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout,
+                            const int32_t* row_idx, const int32_t* row_cnt,
+                            const int32_t* col_idx, const int32_t* col_cnt, float scale, void* dq,
+                            void* dk, void* dv, float* delta, int32_t* status, cudaStream_t st) {
+  const long long rows = (long long)g.BH * g.N;
+  constexpr int RPB = 256 / (D / 8);
+  bwd_delta_kernel<D><<<static_cast<unsigned>((rows + RPB - 1) / RPB), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), rows, delta);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (make_tmap_bf16(&tq, q, g.BH, g.N, D, kBM) != 0 || make_tmap_bf16(&tk, k, g.BH, g.N, D, kBN) != 0 ||
+      make_tmap_bf16(&tv, v, g.BH, g.N, D, kBN) != 0 ||
+      make_tmap_bf16(&tdo, dout, g.BH, g.N, D, kBM) != 0)
+    return cudaErrorInvalidValue;
+  const float scale_log2 = scale * kLog2e;
+
+  e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           DkdvCfg<D>::smem_alloc);
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mk), kThreads,
+                       DkdvCfg<D>::smem_alloc, st>>>(
+      tq, tk, tv, tdo, lse, delta, col_idx, col_cnt, g.N, g.Mq, g.Mk, scale, scale_log2,
+      static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           DqCfg<D>::smem_alloc);
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mq), kThreads, DqCfg<D>::smem_alloc,
+                     st>>>(tq, tk, tv, tdo, lse, delta, row_idx, row_cnt, g.N, g.Mq, g.Mk, scale,
+                           scale_log2, static_cast<__nv_bfloat16*>(dq), status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const Geom& g, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout,
+                            const int32_t* row_idx, const int32_t* row_cnt,
+                            const int32_t* col_idx, const int32_t* col_cnt, float scale, void* dq,
+                            void* dk, void* dv, float* delta, int32_t* status, cudaStream_t st) {
+  if (g.d == 128)
+    return launch_bwd_impl<128>(g, q, k, v, o, lse, dout, row_idx, row_cnt, col_idx, col_cnt,
+                                scale, dq, dk, dv, delta, status, st);
+  return launch_bwd_impl<64>(g, q, k, v, o, lse, dout, row_idx, row_cnt, col_idx, col_cnt, scale,
+                             dq, dk, dv, delta, status, st);
+}
+
+}  // namespace sparge

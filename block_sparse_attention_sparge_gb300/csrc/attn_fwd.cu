@@ -1,0 +1,373 @@
+// Block-sparse attention forward on sm_103a (tcgen05 + TMEM + TMA).
+//
+// Method: mindverse page "Optimierung der Effizienz von Video-Diffusionsmodellen
+// durch SpargeAttention2", sections "Block-duennbesetzte Aufmerksamkeit" (the
+// mask is constant over each tile; a tile is kept whole or dropped whole) and
+// "Effiziente Kernel-Implementierung und Modellanpassung" (masked matmuls and
+// softmax are skipped).  Each query token's softmax runs over the tokens of
+// its q-block's kept kv-blocks only.
+//
+// One CTA computes one 128-token q-block of one head, looping over its CSR
+// list of kept 64-token kv-blocks:
+//   warp 4 (lane 0)  TMA producer: Q once, then K_j / V_j into a ring of stages.
+//   warp 5 (lane 0)  MMA issuer:   S_t = Q K_t^T into a double-buffered TMEM
+//                    tile (128 x 64 fp32), and O += P_t V_t into a TMEM
+//                    accumulator (128 x d fp32).  S_{t+1} is issued before
+//                    waiting for P_t so the tensor core overlaps the softmax.
+//   warps 0-3        softmax: thread r owns query row r (= TMEM lane r).  It
+//                    reads S_t, masks the ragged kv tail, keeps the running
+//                    max m and sum l in base 2, writes P_t (bf16) into shared
+//                    memory in the 128-byte-swizzled K-major layout the MMA
+//                    reads, and finally scales O by 1/l.  O is rescaled in
+//                    TMEM only when the running max grows by more than 8 (a
+//                    factor 256); below that the stale max stays exact
+//                    because the same max is used for l and for O.
+// Every barrier wait is bounded; a timeout records SPARGE_ERR_TIMEOUT.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sparge {
+
+namespace {
+
+constexpr int kBM = 128;         // q-block rows
+constexpr int kBN = 64;          // kv-block rows
+constexpr int kFwdThreads = 192; // 4 softmax warps + producer + MMA
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NST = 3;                       // K/V stages
+  static constexpr int NP = 2;                        // P buffers
+  static constexpr int KCH = D / 64;                  // 128-byte chunks per row
+  static constexpr uint32_t kQ = kBM * D * 2;
+  static constexpr uint32_t kKV = kBN * D * 2;
+  static constexpr uint32_t kP = kBM * kBN * 2;
+  static constexpr uint32_t off_q = 0;
+  static constexpr uint32_t off_k = off_q + kQ;
+  static constexpr uint32_t off_v = off_k + NST * kKV;
+  static constexpr uint32_t off_p = off_v + NST * kKV;
+  static constexpr uint32_t off_bar = off_p + NP * kP;
+  // barriers
+  static constexpr int B_Q = 0;
+  static constexpr int B_KF = 1;
+  static constexpr int B_VF = B_KF + NST;
+  static constexpr int B_KE = B_VF + NST;
+  static constexpr int B_SF = B_KE + NST;
+  static constexpr int B_PF = B_SF + 2;
+  static constexpr int B_PV = B_PF + NP;
+  static constexpr int B_DRAIN = B_PV + 2;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr uint32_t off_tmem_slot = off_bar + NBAR * 8;
+  static constexpr uint32_t bytes = off_tmem_slot + 16;
+  static constexpr uint32_t smem_alloc = bytes + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t tmem_cols = 256;            // S0 [0,64) S1 [64,128) O [128,128+D)
+  static constexpr uint32_t col_s = 0;
+  static constexpr uint32_t col_o = 128;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ row_idx,
+                    const int32_t* __restrict__ row_cnt, int N, int Mq, int Mk, float scale_log2,
+                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                    int32_t* __restrict__ status) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t s0 = smem_u32(sm);
+  auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::off_tmem_slot);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x / Mq;
+  const int qb = blockIdx.x % Mq;
+  const long long row_id = (long long)bh * Mq + qb;
+  const int n = min(max(__ldg(row_cnt + row_id), 0), Mk);
+  const int32_t* list = row_idx + row_id * Mk;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i)
+      mbar_init(bar(i), (i >= C::B_PF && i < C::B_PF + C::NP) ? 128u : 1u);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(bar(C::B_Q), C::kQ);
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_3d(s0 + C::off_q + c * kBM * 128, &tmQ, bar(C::B_Q), c * 64, qb * kBM, bh);
+      int issued = 0;
+      for (int t = 0; t < n; ++t) {
+        const int s = t % C::NST;
+        if (t >= C::NST && !mbar_wait(bar(C::B_KE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+          report_error(status, SPARGE_ERR_TIMEOUT);
+          break;
+        }
+        const int j = min(max(__ldg(list + t), 0), Mk - 1);
+        mbar_arrive_expect_tx(bar(C::B_KF + s), C::kKV);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(s0 + C::off_k + s * C::kKV + c * kBN * 128, &tmK, bar(C::B_KF + s), c * 64,
+                      j * kBN, bh);
+        mbar_arrive_expect_tx(bar(C::B_VF + s), C::kKV);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(s0 + C::off_v + s * C::kKV + c * kBN * 128, &tmV, bar(C::B_VF + s), c * 64,
+                      j * kBN, bh);
+        issued = t + 1;
+      }
+      // Let the last loads land before the CTA can exit (they complete on their own).
+      for (int t = max(0, issued - C::NST); t < issued; ++t) {
+        const int s = t % C::NST;
+        mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs);
+        mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
+      bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
+      for (int t = 0; ok && t <= n; ++t) {
+        if (t < n) {
+          const int s = t % C::NST;
+          if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kbase = s0 + C::off_k + s * C::kKV;
+          const uint32_t dS = tmem + C::col_s + (t & 1) * kBN;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk & 3) * 32;
+            const uint64_t a = sdesc_sw128(s0 + C::off_q + (kk >> 2) * (kBM * 128) + koff, 16, 1024);
+            const uint64_t b = sdesc_sw128(kbase + (kk >> 2) * (kBN * 128) + koff, 16, 1024);
+            tc_mma_bf16(dS, a, b, idS, kk > 0);
+          }
+          tc_commit(bar(C::B_SF + (t & 1)));
+        }
+        if (t >= 1) {
+          const int u = t - 1;
+          const int su = u % C::NST;
+          const int pb = u % C::NP;
+          if (!mbar_wait(bar(C::B_PF + pb), (u / C::NP) & 1, kWaitTimeoutNs) ||
+              !mbar_wait(bar(C::B_VF + su), (u / C::NST) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t pbase = s0 + C::off_p + pb * C::kP;
+          const uint32_t vbase = s0 + C::off_v + su * C::kKV;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(pbase + kk * 32, 16, 1024);
+            const uint64_t b = sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024);
+            tc_mma_bf16(tmem + C::col_o, a, b, idO, (u > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_KE + su));
+          tc_commit(bar(C::B_PV + (u & 1)));
+        }
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+      // Drain: every MMA issued above has completed once this arrives.
+      tc_commit(bar(C::B_DRAIN));
+      mbar_wait(bar(C::B_DRAIN), 0, kWaitTimeoutNs);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = threadIdx.x;  // 0..127 == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int row = qb * kBM + r;
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[kBN];
+      {
+        uint32_t ra[16], rb[16], rc[16], rd[16];
+        const uint32_t sa = lane_base + C::col_s + (t & 1) * kBN;
+        SPARGE_TMEM_LD_X16(sa + 0, ra);
+        SPARGE_TMEM_LD_X16(sa + 16, rb);
+        SPARGE_TMEM_LD_X16(sa + 32, rc);
+        SPARGE_TMEM_LD_X16(sa + 48, rd);
+        SPARGE_TMEM_WAIT_LD16(ra);
+        SPARGE_TMEM_WAIT_LD16(rb);
+        SPARGE_TMEM_WAIT_LD16(rc);
+        SPARGE_TMEM_WAIT_LD16(rd);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          x[c] = __uint_as_float(ra[c]) * scale_log2;
+          x[16 + c] = __uint_as_float(rb[c]) * scale_log2;
+          x[32 + c] = __uint_as_float(rc[c]) * scale_log2;
+          x[48 + c] = __uint_as_float(rd[c]) * scale_log2;
+        }
+      }
+      const int j = min(max(__ldg(list + t), 0), Mk - 1);
+      const int valid = N - j * kBN;
+      if (valid < kBN) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c >= valid) x[c] = -INFINITY;
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int c = 1; c < kBN; ++c) mt = fmaxf(mt, x[c]);
+      const float m_new = fmaxf(m_used, mt);
+      // Rescale decision must be warp-uniform (tcgen05.ld/st are warp-wide).
+      const bool want = (t > 0) && (m_new - m_used > kRescaleLog2);
+      if (t == 0) m_used = m_new;
+      if (__any_sync(0xffffffffu, want)) {
+        // O holds every PV up to t-1 once that commit has arrived.
+        if (!warp_wait(bar(C::B_PV + ((t - 1) & 1)), ((t - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = want ? exp2f(m_used - m_new) : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t ro[16];
+          SPARGE_TMEM_LD_X16(lane_base + C::col_o + c0, ro);
+          SPARGE_TMEM_WAIT_LD16(ro);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) ro[c] = __float_as_uint(__uint_as_float(ro[c]) * alpha);
+          SPARGE_TMEM_ST_X16(lane_base + C::col_o + c0, ro);
+        }
+        tmem_st_wait();
+        if (want) {
+          l *= alpha;
+          m_used = m_new;
+        }
+      }
+      // P buffer t % NP is free once PV(t - NP) has completed.
+      if (t >= C::NP) {
+        const int u = t - C::NP;
+        if (!warp_wait(bar(C::B_PV + (u & 1)), (u >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+      }
+      uint8_t* prow = sm + C::off_p + (t % C::NP) * C::kP;
+      float rs = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = exp2f(x[ch * 8 + e] - m_used);
+          rs += p[e];
+        }
+        uint4 v;
+        v.x = pack_bf16x2(p[0], p[1]);
+        v.y = pack_bf16x2(p[2], p[3]);
+        v.z = pack_bf16x2(p[4], p[5]);
+        v.w = pack_bf16x2(p[6], p[7]);
+        *reinterpret_cast<uint4*>(prow + sw128_offset(r, ch * 16)) = v;
+      }
+      l += rs;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PF + (t % C::NP)));
+    }
+    if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+    // ---------------------------------------------------------- epilogue
+    const bool have = ok && n > 0 && warp_wait(bar(C::B_PV + ((n - 1) & 1)), ((n - 1) >> 1) & 1);
+    if (ok && n > 0 && !have) report_error(status, SPARGE_ERR_TIMEOUT);
+    tc_fence_after();
+    const float inv_l = (have && l > 0.f) ? 1.f / l : 0.f;
+    __nv_bfloat16* orow = out + ((long long)bh * N + row) * D;
+    const bool in_range = row < N;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      uint32_t ro[16];
+      if (have) {
+        SPARGE_TMEM_LD_X16(lane_base + C::col_o + c0, ro);
+        SPARGE_TMEM_WAIT_LD16(ro);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) ro[c] = 0u;
+      }
+      uint4 w0, w1;
+      w0.x = pack_bf16x2(__uint_as_float(ro[0]) * inv_l, __uint_as_float(ro[1]) * inv_l);
+      w0.y = pack_bf16x2(__uint_as_float(ro[2]) * inv_l, __uint_as_float(ro[3]) * inv_l);
+      w0.z = pack_bf16x2(__uint_as_float(ro[4]) * inv_l, __uint_as_float(ro[5]) * inv_l);
+      w0.w = pack_bf16x2(__uint_as_float(ro[6]) * inv_l, __uint_as_float(ro[7]) * inv_l);
+      w1.x = pack_bf16x2(__uint_as_float(ro[8]) * inv_l, __uint_as_float(ro[9]) * inv_l);
+      w1.y = pack_bf16x2(__uint_as_float(ro[10]) * inv_l, __uint_as_float(ro[11]) * inv_l);
+      w1.z = pack_bf16x2(__uint_as_float(ro[12]) * inv_l, __uint_as_float(ro[13]) * inv_l);
+      w1.w = pack_bf16x2(__uint_as_float(ro[14]) * inv_l, __uint_as_float(ro[15]) * inv_l);
+      if (in_range) {
+        *reinterpret_cast<uint4*>(orow + c0) = w0;
+        *reinterpret_cast<uint4*>(orow + c0 + 8) = w1;
+      }
+    }
+    if (lse != nullptr && in_range)
+      lse[(long long)bh * N + row] =
+          (have && l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::tmem_cols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_impl(const Geom& g, const void* q, const void* k, const void* v,
+                            const int32_t* row_idx, const int32_t* row_cnt, float scale, void* o,
+                            float* lse, int32_t* status, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (make_tmap_bf16(&tq, q, g.BH, g.N, D, kBM) != 0 || make_tmap_bf16(&tk, k, g.BH, g.N, D, kBN) != 0 ||
+      make_tmap_bf16(&tv, v, g.BH, g.N, D, kBN) != 0)
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_alloc);
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  const unsigned grid = static_cast<unsigned>((long long)g.BH * g.Mq);
+  attn_fwd_kernel<D><<<grid, kFwdThreads, C::smem_alloc, st>>>(
+      tq, tk, tv, row_idx, row_cnt, g.N, g.Mq, g.Mk, scale_log2,
+      static_cast<__nv_bfloat16*>(o), lse, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const void* v,
+                            const int32_t* row_idx, const int32_t* row_cnt, float scale, void* o,
+                            float* lse, int32_t* status, cudaStream_t st) {
+  if (g.d == 128) return launch_fwd_impl<128>(g, q, k, v, row_idx, row_cnt, scale, o, lse, status, st);
+  return launch_fwd_impl<64>(g, q, k, v, row_idx, row_cnt, scale, o, lse, status, st);
+}
+
+}  // namespace sparge

@@ -1,0 +1,54 @@
+// Host-side launch functions of the sm_103a kernels (internal to libsparge).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "sparge.h"
+
+namespace sparge {
+
+// Geometry derived from a validated sparge_shape.
+struct Geom {
+  int B, H, N, d, bq, bk;
+  int BH, Mq, Mk, Mkw;  // Mkw = ceil(Mk / 32) bitmask words per row
+};
+
+Geom make_geom(const sparge_shape& s);
+
+// Rows of the pooled map one selection CTA handles (fits its logits in smem).
+int select_rows_per_cta(int Mk);
+
+// pool.cu / mask.cu
+cudaError_t launch_pool(const Geom& g, const void* q, const void* k, float* qbar, float* kbar,
+                        float* kbarT, cudaStream_t st);
+cudaError_t launch_score_select(const Geom& g, const float* qbar, const float* kbarT, float scale,
+                                int ktop, float p, uint32_t* bitmask, int32_t* row_idx,
+                                int32_t* row_cnt, float* logit_out, float* prob_out,
+                                cudaStream_t st);
+cudaError_t launch_select_from_prob(const Geom& g, const float* prob, int ktop, float p,
+                                    uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
+                                    cudaStream_t st);
+cudaError_t launch_csc(const Geom& g, const uint32_t* bitmask, int32_t* col_idx, int32_t* col_cnt,
+                       cudaStream_t st);
+
+// attn_fwd.cu
+cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const void* v,
+                            const int32_t* row_idx, const int32_t* row_cnt, float scale, void* o,
+                            float* lse, int32_t* status, cudaStream_t st);
+
+// attn_bwd.cu
+cudaError_t launch_attn_bwd(const Geom& g, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout,
+                            const int32_t* row_idx, const int32_t* row_cnt,
+                            const int32_t* col_idx, const int32_t* col_cnt, float scale, void* dq,
+                            void* dk, void* dv, float* delta, int32_t* status, cudaStream_t st);
+
+// api.cu
+cudaError_t launch_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
+
+// tma.cu: 3-D bf16 tensor map over [BH, N, d] with a (64 x box_rows) 128-byte-swizzled box.
+int make_tmap_bf16(void* tmap_out, const void* base, int BH, int N, int d, int box_rows);
+
+}  // namespace sparge

@@ -1,0 +1,186 @@
+/*
+ * sparge.h -- C ABI of the GB300 (sm_103a) SpargeAttention2 hot path.
+ *
+ * The method (hybrid Top-k+Top-p block-sparse attention) is described on the
+ * mindverse page "Optimierung der Effizienz von Video-Diffusionsmodellen durch
+ * SpargeAttention2" (cited below as [P4] with its section name) and in the
+ * abstract of "SpargeAttention2: Trainable Sparse Attention via Hybrid
+ * Top-k+Top-p Masking and Distillation Fine-Tuning" ([P2] "Abstract").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16, shape [B, H, N, d], dense
+ *   row-major (d innermost), in device memory, 16-byte aligned.
+ * - Blocks: block_q query tokens by block_kv key tokens.  Mq = ceil(N/block_q),
+ *   Mk = ceil(N/block_kv).  The last block of each may be partial.
+ * - The caller owns every buffer and the stream.  The library allocates,
+ *   frees and synchronises nothing (sparge_read_status excepted, which
+ *   synchronises the given stream), and keeps no global mutable state.
+ * - All launches are asynchronous on `stream` (NULL = the legacy default
+ *   stream).  Arguments are validated before any launch; on an error nothing
+ *   is launched and a negative status is returned.
+ * - `status` (nullable) is a device int32 the caller zeroes before use.  A
+ *   kernel that gives up on a bounded internal wait writes SPARGE_ERR_TIMEOUT
+ *   there (first error wins) and returns instead of hanging.  Read it with
+ *   sparge_read_status.
+ * - softmax_scale 0 means 1/sqrt(d).
+ */
+#ifndef SPARGE_H_
+#define SPARGE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* sparge_stream_t;
+
+/* Status codes returned by every entry point. */
+enum sparge_status {
+  SPARGE_OK = 0,
+  SPARGE_ERR_INVALID_ARG = -1, /* null pointer, bad size, k/p out of range  */
+  SPARGE_ERR_UNSUPPORTED = -2, /* d or block size this build does not offer */
+  SPARGE_ERR_MISALIGNED = -3,  /* a tensor pointer not 16-byte aligned      */
+  SPARGE_ERR_WORKSPACE = -4,   /* workspace null or too small               */
+  SPARGE_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed         */
+  SPARGE_ERR_TIMEOUT = -6      /* a device-side bounded wait gave up        */
+};
+
+/* Problem shape.  Supported: d in {64, 128}; block_q = 128; block_kv = 64;
+ * 1 <= N <= 524288 (so Mk <= 8192); B*H >= 1. */
+typedef struct sparge_shape {
+  int32_t B, H, N, d;
+  int32_t block_q, block_kv;
+} sparge_shape;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int sparge_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sparge_status_string(int status);
+
+/*
+ * sparge_pool -- step 1 of the mask: per-block mean of Q and of K.
+ * [P4 "Maskierungsstrategien: Top-k und Top-p"]: the mask is chosen on a
+ * block-pooled attention map; the pooling is the mean over each block's
+ * valid tokens.
+ *   q, k  : bf16 [B,H,N,d] (device).
+ *   qbar  : fp32 [B,H,Mq,d] out (device).  kbar: fp32 [B,H,Mk,d] out (device).
+ * Either output may be NULL (then it is not computed).
+ */
+int sparge_pool(const sparge_shape* shape, const void* q, const void* k, float* qbar,
+                float* kbar, sparge_stream_t stream);
+
+/* Workspace bytes sparge_mask needs (pooled Q and K, fp32). */
+int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes);
+
+/*
+ * sparge_mask -- block mask construction, steps 1-3 of the hot path.
+ * [P4 "Maskierungsstrategien: Top-k und Top-p"], [P4 "Hybride Top-k+Top-p
+ * Maskierung"], [P4 "Effiziente Kernel-Implementierung und Modellanpassung"].
+ *   1. qbar_i, kbar_j = block means of Q and K (as sparge_pool).
+ *   2. L_ij = scale * <qbar_i, kbar_j>;  P_i. = softmax_j(L_i.)  (fp32).
+ *   3. Per row i, order blocks by P descending, ties by lower index.
+ *      K   = clamp(ceil(k_frac*Mk - 1e-4), 1, Mk)           (Top-k count)
+ *      m_p = smallest m with fl64(sum of the first m u_j) >= fl64(p * U),
+ *            u_j = floor(P_ij * 2^40), U = sum_j u_j       (Top-p count)
+ *            (p <= 0: m_p = 0; p >= 1: m_p = Mk)
+ *      keep the first max(K, m_p) blocks (= Top-k set union Top-p set).
+ * Arguments:
+ *   q, k         : bf16 [B,H,N,d] (device).
+ *   k_frac       : in (0, 1]; p in [0, 1] (p = 0 switches Top-p off).
+ *   bitmask      : uint32 [B,H,Mq,ceil(Mk/32)] out; block j of row i is bit
+ *                  j%32 of word j/32.  Required.
+ *   row_idx      : int32 [B,H,Mq,Mk] out; the first row_cnt[i] entries of row
+ *                  i are its kept kv-blocks in ascending order; the rest are
+ *                  left unwritten.  Required.
+ *   row_cnt      : int32 [B,H,Mq] out.  Required.
+ *   col_idx/cnt  : int32 [B,H,Mk,Mq] / [B,H,Mk] out; the transposed lists
+ *                  (kept q-blocks per kv-block, ascending).  Both NULL or both
+ *                  set; needed by sparge_attn_bwd.
+ *   pooled_logit : fp32 [B,H,Mq,Mk] out, L (nullable).
+ *   pooled_prob  : fp32 [B,H,Mq,Mk] out, P (nullable).
+ *   workspace    : device buffer of sparge_mask_workspace_bytes bytes.
+ * The mask is a deterministic function of the fp32 P it computes.
+ */
+int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k_frac, float p,
+                float softmax_scale, uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
+                int32_t* col_idx, int32_t* col_cnt, float* pooled_logit, float* pooled_prob,
+                void* workspace, size_t ws_bytes, int32_t* status, sparge_stream_t stream);
+
+/*
+ * sparge_mask_from_prob -- step 3 alone: the hybrid selection of sparge_mask
+ * applied to a caller-supplied pooled probability map.
+ *   prob : fp32 [B,H,Mq,Mk] (device), each entry in [0, 1].
+ * Other arguments and outputs as in sparge_mask.  Given the same P, the mask
+ * equals the one sparge_mask emits.
+ */
+int sparge_mask_from_prob(const sparge_shape* shape, const float* prob, float k_frac, float p,
+                          uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
+                          int32_t* col_idx, int32_t* col_cnt, int32_t* status,
+                          sparge_stream_t stream);
+
+/*
+ * sparge_attn_fwd -- block-sparse attention forward, step 4.
+ * [P4 "Grundlagen der duennbesetzten Aufmerksamkeit und ihre
+ * Herausforderungen"], [P4 "Block-duennbesetzte Aufmerksamkeit"], [P4
+ * "Effiziente Kernel-Implementierung und Modellanpassung"]: only the kept
+ * (q-block, kv-block) tiles are computed; the softmax of each query token is
+ * normalised over the tokens of its kept kv-blocks.  No causal mask.
+ *   O_t   = sum_u softmax_u(scale * Q_t.K_u) V_u  over kept tokens u
+ *   LSE_t = log sum_u exp(scale * Q_t.K_u)
+ * Arguments:
+ *   q, k, v          : bf16 [B,H,N,d] (device).
+ *   row_idx, row_cnt : the CSR lists of sparge_mask (device); every index in
+ *                      [0, Mk), counts in [0, Mk].
+ *   o                : bf16 [B,H,N,d] out.  lse: fp32 [B,H,N] out (nullable).
+ * A q-block with row_cnt 0 gets O = 0 and LSE = -inf.
+ */
+int sparge_attn_fwd(const sparge_shape* shape, const void* q, const void* k, const void* v,
+                    const int32_t* row_idx, const int32_t* row_cnt, float softmax_scale,
+                    void* o, float* lse, int32_t* status, sparge_stream_t stream);
+
+/* Workspace bytes sparge_attn_bwd needs (fp32 D = rowsum(dO*O) per token). */
+int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
+
+/*
+ * sparge_attn_bwd -- gradients of sparge_attn_fwd, step 5.
+ * [P2 "Abstract"] (trainable sparse attention), [P4 "Effiziente
+ * Kernel-Implementierung und Modellanpassung"] (forward and backward skip
+ * masked tiles).  The mask is a constant; for the kept tiles:
+ *   P = exp(scale*Q K^T - LSE), D = rowsum(dO * O), dS = P * (dO V^T - D),
+ *   dV = P^T dO, dQ = scale * dS K, dK = scale * dS^T Q.
+ * Arguments:
+ *   q, k, v, o, dout : bf16 [B,H,N,d] (device); o and lse from sparge_attn_fwd.
+ *   lse              : fp32 [B,H,N] (device).
+ *   row_idx/cnt, col_idx/cnt : CSR and CSC lists from sparge_mask (device).
+ *   dq, dk, dv       : bf16 [B,H,N,d] out.  Tokens of kv-blocks no q-block
+ *                      keeps get dK = dV = 0.
+ *   workspace        : device buffer of sparge_attn_bwd_workspace_bytes bytes.
+ * Deterministic (no atomics).
+ */
+int sparge_attn_bwd(const sparge_shape* shape, const void* q, const void* k, const void* v,
+                    const void* o, const float* lse, const void* dout, const int32_t* row_idx,
+                    const int32_t* row_cnt, const int32_t* col_idx, const int32_t* col_cnt,
+                    float softmax_scale, void* dq, void* dk, void* dv, void* workspace,
+                    size_t ws_bytes, int32_t* status, sparge_stream_t stream);
+
+/* Copies the device status word to *host_status after synchronising `stream`. */
+int sparge_read_status(const int32_t* status, sparge_stream_t stream, int32_t* host_status);
+
+/*
+ * sparge_debug_wait_probe -- launches one CTA that waits on a barrier nothing
+ * ever arrives at, with the given limit (clamped to 1 ms .. 5 s).  It must
+ * record SPARGE_ERR_TIMEOUT in `status` and return: a test of the bounded-wait
+ * path that never hangs the GPU.
+ */
+int sparge_debug_wait_probe(int32_t* status, uint64_t timeout_ns, sparge_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARGE_H_ */
