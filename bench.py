@@ -1,0 +1,502 @@
+"""Benchmark of the SpargeAttention2 hot path on GB300.
+
+One step = the whole hot path on one batch of synthetic input: block mask
+(pool + pooled map + hybrid Top-k/Top-p selection + CSC lists), block-sparse
+attention forward, and backward (dQ, dK, dV).  Default workload: the
+Wan2.1-1.3B 480p attention shape, B=1, H=12, N=32760 (21x30x52 latents),
+d=128, 128x64 blocks, k=5% with Top-p off (p=0): exactly 26 of 512 kv-blocks
+per row, 94.92% sparsity.  The hybrid rule at the workload's p=0.9 is timed
+too and reported under "hybrid".
+
+Prints one JSON line (rank 0).  ``value`` = kept-FLOP TFLOP/s of fwd+bwd
+(algorithmic FLOPs 4*d and 10*d per kept valid query x key pair) divided by
+the device time of the whole step, mask included.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload (heads are
+independent; weak scaling, no data-path collective); the step time is the
+max over ranks.  ``--impl reference`` times the CPU oracle (a bounded sample
+of the same workload per step) on the host cores; there is no other
+reference implementation of this method.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("sparse attn fwd+bwd ms & kept-FLOP TFLOP/s at 95% sparsity; "
+          "% of BF16/HBM roofline")
+KERNELS_PER_STEP = 7  # pool, score+select, csc, fwd, delta, dkdv, dq
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, group_backend_ready: bool):
+    """Max over ranks (identity on one process)."""
+    if not group_backend_ready:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, group_backend_ready: bool):
+    if not group_backend_ready:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(local_ms: float, local_flops: float, steps: int, distributed: bool):
+    """Whole-job throughput: FLOPs of all ranks / the slowest rank's time."""
+    t_ms = reduce_max(local_ms, distributed)
+    flops = reduce_sum(local_flops, distributed)
+    return t_ms, flops * steps / (t_ms * 1e-3) / 1e12
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_index], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, parts))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [p for ts, p in rows if t0 - 1.0 <= ts <= t1 + 1.0] or [p for _, p in rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(p[2]) for p in inside if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for p in inside if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[6 + i] == "Active"})
+        pw = [float(p[4]) for p in inside if p[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons,
+                "samples": len(inside),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------------------- workload math
+def kept_pairs(mask_bool, n, bq, bk):
+    """Sum over kept (q-block, kv-block) tiles of valid-query x valid-key counts."""
+    import torch
+    mq, mk = mask_bool.shape[-2], mask_bool.shape[-1]
+    rq = torch.full((mq,), bq, dtype=torch.float64, device=mask_bool.device)
+    rq[-1] = n - (mq - 1) * bq
+    rk = torch.full((mk,), bk, dtype=torch.float64, device=mask_bool.device)
+    rk[-1] = n - (mk - 1) * bk
+    return float((mask_bool.double() * rq[:, None] * rk[None, :]).sum().item())
+
+
+def unpack_bits(bitmask, mk):
+    import torch
+    w = bitmask.to(torch.int64) & 0xFFFFFFFF
+    bits = (w[..., :, None] >> torch.arange(32, device=w.device)) & 1
+    return bits.reshape(*w.shape[:-1], -1)[..., :mk].bool()
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+def oracle_sample(host, wl, h, qblocks, k_frac, p):
+    """Runs the CPU oracle on a bounded sample of the workload: pooled map of
+    head h (all kv-blocks, the sampled q-blocks), hybrid selection of those
+    rows, and block-gather fwd + bwd (fp32) of those q-blocks.  Returns
+    (seconds, kept fwd+bwd FLOPs of the sample)."""
+    import numpy as np
+    import oracle as O
+    q, k, v, do = host
+    n, d = wl.N, wl.d
+    mq, mk = O.num_blocks(n, wl.block_q), O.num_blocks(n, wl.block_kv)
+    i0, i1 = qblocks[0], qblocks[-1] + 1
+    t0 = time.perf_counter()
+    kbar = O.pool_blocks(k[h][None, None], wl.block_kv)
+    qbar = O.pool_blocks(q[h, i0 * wl.block_q:min(n, i1 * wl.block_q)][None, None], wl.block_q)
+    prob = O.row_softmax(O.pooled_logits(qbar, kbar, 1.0 / math.sqrt(d)))
+    rows = O.hybrid_mask_from_prob(prob.astype(np.float32), k_frac, p)
+    mask = np.zeros((1, 1, mq, mk), dtype=bool)
+    mask[0, 0, i0:i1] = rows[0, 0]
+    qs, ks, vs, dos = (x[h][None, None] for x in (q, k, v, do))
+    O.sparse_attention_blocks(qs, ks, vs, mask, wl.block_q, wl.block_kv, dtype=np.float32,
+                              qblocks=list(qblocks))
+    O.sparse_attention_blocks_bwd(qs, ks, vs, dos, mask, wl.block_q, wl.block_kv,
+                                  dtype=np.float32, qblocks=list(qblocks))
+    dt = time.perf_counter() - t0
+    rq = np.array([min(wl.block_q, n - i * wl.block_q) for i in range(i0, i1)], dtype=np.float64)
+    rk = np.array([min(wl.block_kv, n - j * wl.block_kv) for j in range(mk)], dtype=np.float64)
+    pairs = float((rows[0, 0] * rq[:, None] * rk[None, :]).sum())
+    return dt, 14.0 * d * pairs
+
+
+def host_inputs(tensors, heads):
+    import numpy as np
+    return tuple(t[0, :heads].float().cpu().numpy().astype(np.float32) for t in tensors)
+
+
+def cpu_baseline(host, wl, k_frac, p, seconds: float):
+    """Times the oracle as it stands for about `seconds` of CPU work."""
+    mq = -(-wl.N // wl.block_q)
+    total_t = total_f = 0.0
+    h = i = 0
+    nblk = 4
+    while total_t < seconds:
+        qb = [(i + x) % mq for x in range(nblk)]
+        qb = sorted(set(qb))
+        if qb[-1] - qb[0] + 1 != len(qb):
+            qb = list(range(qb[0], mq))
+        dt, fl = oracle_sample(host, wl, h % host[0].shape[0], qb, k_frac, p)
+        total_t += dt
+        total_f += fl
+        i += nblk
+        h += 1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": (f"{total_t:.1f} s of the NumPy oracle on the host: per sample, head pooling "
+                       f"+ pooled map + hybrid selection + fp32 block-gather fwd+bwd of {nblk} "
+                       f"q-blocks of one {wl.name} head (BLAS threads: library default)"),
+            "seconds": round(total_t, 2)}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, wl, k_frac, p):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    import torch
+    from block_sparse_attention_sparge_gb300 import synth
+    tens = synth.video_inputs(wl, device="cpu", heads=2)
+    host = host_inputs(tens, 2)
+    mq = -(-wl.N // wl.block_q)
+    # calibrate the sample so (steps + warmup) samples take about 90 s
+    dt1, _ = oracle_sample(host, wl, 0, [0], k_frac, p)
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    nblk = int(max(1, min(16, per_step / max(dt1, 1e-3))))
+    times, flops = [], []
+    for s in range(args.warmup + args.steps):
+        i0 = (s * nblk) % max(1, mq - nblk)
+        dt, fl = oracle_sample(host, wl, s % 2, list(range(i0, i0 + nblk)), k_frac, p)
+        if s >= args.warmup:
+            times.append(dt)
+            flops.append(fl)
+    tot_t, tot_f = sum(times), sum(flops)
+    value = tot_f / tot_t / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(wl, k_frac, p, None),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {nblk} q-block(s) of one head (pool, map, select, "
+                                   f"fwd, bwd), NumPy fp32 block-gather oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+    return 0
+
+
+def workload_config(wl, k_frac, p, sparsity):
+    return {"workload": (f"{wl.name}: Wan2.1-shaped attention fwd+bwd, B={wl.B}, H={wl.H}, "
+                         f"N={wl.N} ({'x'.join(map(str, wl.grid))}), d={wl.d}, "
+                         f"blocks {wl.block_q}x{wl.block_kv}, k={k_frac:g}, p={p:g}"),
+            "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "block_q": wl.block_q,
+            "block_kv": wl.block_kv, "k_frac": k_frac, "p": p, "sparsity": sparsity,
+            "l2": "inputs larger than L2 (Q, K, V, dO: 403 MB per step vs 129 MB L2)"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, wl, k_frac, p):
+    import torch
+    import torch.distributed as dist
+    from block_sparse_attention_sparge_gb300 import binding as B
+    from block_sparse_attention_sparge_gb300 import synth
+
+    ws, rank, local = dist_info()
+    distributed = ws > 1
+    if distributed:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if distributed else 0)
+    torch.cuda.set_device(dev)
+    B.load_library()
+
+    q, k, v, do = synth.video_inputs(wl, device=dev)
+    Bn, H, N, d = q.shape
+    mq, mk = -(-N // wl.block_q), -(-N // wl.block_kv)
+    stream = torch.cuda.current_stream(dev)
+
+    # persistent buffers: no allocation inside the timed loop
+    mask_out = B._mask_outputs(Bn, H, mq, mk, dev, True)
+    import ctypes
+    shp = B.Shape(Bn, H, N, d, wl.block_q, wl.block_kv)
+    nb = ctypes.c_size_t(0)
+    B.load_library().sparge_mask_workspace_bytes(ctypes.byref(shp), ctypes.byref(nb))
+    ws_mask = torch.empty(nb.value, dtype=torch.uint8, device=dev)
+    B.load_library().sparge_attn_bwd_workspace_bytes(ctypes.byref(shp), ctypes.byref(nb))
+    ws_bwd = torch.empty(nb.value, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((Bn, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(kf, pp, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        res = B.sparge_mask(q, k, kf, pp, out=mask_out, workspace=ws_mask)
+        if ev is not None:
+            ev[1].record(stream)
+        B.sparge_attn_fwd(q, k, v, res["row_idx"], res["row_cnt"], out=o, lse=lse, status=status)
+        if ev is not None:
+            ev[2].record(stream)
+        B.sparge_attn_bwd(q, k, v, o, lse, do, res["row_idx"], res["row_cnt"], res["col_idx"],
+                          res["col_cnt"], out=(dq, dk, dv), workspace=ws_bwd, status=status)
+        if ev is not None:
+            ev[3].record(stream)
+        return res
+
+    # work per step from the mask this rule produces
+    res = step(k_frac, p)
+    torch.cuda.synchronize()
+    maskb = unpack_bits(mask_out["bitmask"], mk)
+    pairs = kept_pairs(maskb, N, wl.block_q, wl.block_kv)
+    kept_tiles = int(maskb.sum().item())
+    sparsity = 1.0 - kept_tiles / float(Bn * H * mq * mk)
+    fwd_flops = 4.0 * d * pairs
+    bwd_flops = 10.0 * d * pairs
+    step_flops = fwd_flops + bwd_flops
+    mask_bytes = (2.0 * Bn * H * N * d * 2 + Bn * H * mq * ((mk + 31) // 32) * 4
+                  + 2 * kept_tiles * 4 + Bn * H * (mq + mk) * 4)
+
+    for _ in range(args.warmup):
+        step(k_frac, p)
+    torch.cuda.synchronize()
+
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[0] or "0"
+    sampler = ClockSampler(gpu_index)
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if distributed:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for s in range(args.steps):
+        step(k_frac, p, evs[s])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if distributed:
+        dist.barrier()
+    clocks = sampler.stop(wall0, wall1)
+    total_ms = start.elapsed_time(stop)
+    ms_step_local = total_ms / args.steps
+    parts = {"mask": [], "fwd": [], "bwd": []}
+    for e in evs:
+        parts["mask"].append(e[0].elapsed_time(e[1]))
+        parts["fwd"].append(e[1].elapsed_time(e[2]))
+        parts["bwd"].append(e[2].elapsed_time(e[3]))
+    part_ms = {kk: sum(vv) / len(vv) for kk, vv in parts.items()}
+    st = B._read_status(status)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed loop")
+
+    ms_step, value = aggregate(ms_step_local, step_flops, 1, distributed)  # all ranks
+
+    peaks, peak_kind = load_peaks()
+    tc_peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    hbm_peak = float(peaks["hbm_gbs"])
+    roof = {
+        "fwd": {"kernel": "sparge_attn_fwd (attn_fwd_kernel)", "bound": "tensor",
+                "achieved": fwd_flops / (part_ms["fwd"] * 1e-3) / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s"},
+        "bwd": {"kernel": "sparge_attn_bwd (delta + dK/dV + dQ kernels)", "bound": "tensor",
+                "achieved": bwd_flops / (part_ms["bwd"] * 1e-3) / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s"},
+        "mask": {"kernel": "sparge_mask (pool + score/select + csc kernels)", "bound": "hbm",
+                 "achieved": mask_bytes / (part_ms["mask"] * 1e-3) / 1e9, "peak": hbm_peak,
+                 "unit": "GB/s"},
+    }
+    for r in roof.values():
+        r["frac"] = r["achieved"] / r["peak"]
+        r["peak_source"] = (f"{peak_kind} ({'bf16_tflops_sustained' if r['bound'] == 'tensor' else 'hbm_gbs'}"
+                            f" of MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback")
+    dom = max(part_ms, key=part_ms.get)
+    roofline = dict(roof[dom])
+    roofline["traffic"] = None
+    roofline["per_launch_ms"] = part_ms[dom]
+    roofline["algorithmic"] = {"fwd": "4*d per kept valid (query, key) pair",
+                               "bwd": "10*d per kept valid (query, key) pair",
+                               "mask": "Q+K read once + bitmask, CSR/CSC and counts written"}[dom]
+
+    # hybrid rule (the workload's p) on the same inputs
+    hybrid = None
+    if not args.no_hybrid:
+        step(k_frac, wl.p)
+        torch.cuda.synchronize()
+        mb = unpack_bits(mask_out["bitmask"], mk)
+        hp = kept_pairs(mb, N, wl.block_q, wl.block_kv)
+        hs = 1.0 - float(mb.sum().item()) / float(Bn * H * mq * mk)
+        nh = max(3, min(args.steps, 30))
+        for _ in range(2):
+            step(k_frac, wl.p)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(nh):
+            step(k_frac, wl.p)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        hms = e0.elapsed_time(e1) / nh
+        hybrid = {"k_frac": k_frac, "p": wl.p, "sparsity": hs, "ms_per_step": hms,
+                  "tflops": 14.0 * d * hp / (hms * 1e-3) / 1e12, "steps": nh}
+
+    # end to end through the public API: pinned host inputs in, results out
+    nsteps_e2e = 0 if args.no_e2e else max(3, min(args.steps, 20))
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+    outs = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(4)]
+    h2d = 4 * q.numel() * q.element_size()
+    d2h = 4 * q.numel() * q.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for it in range(nsteps_e2e + 1 if nsteps_e2e else 0):
+        if it == 1:
+            e0.record(stream)
+        for src, dst in ((hq, q), (hk, k), (hv, v), (hdo, do)):
+            dst.copy_(src, non_blocking=True)
+        step(k_frac, p)
+        for src, dst in ((o, outs[0]), (dq, outs[1]), (dk, outs[2]), (dv, outs[3])):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if nsteps_e2e:
+        e2e_ms = e0.elapsed_time(e1) / nsteps_e2e
+        e2e_ms, e2e_val = aggregate(e2e_ms, step_flops, 1, distributed)
+    else:
+        e2e_ms = e2e_val = None
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        host = host_inputs((q, k, v, do), 2)
+        cpu = cpu_baseline(host, wl, k_frac, p, args.cpu_seconds)
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded smooth Gaussian Q/K fields + sinks, N(0,1) V/dO)",
+            "config": workload_config(wl, k_frac, p, sparsity),
+            "breakdown_ms": part_ms,
+            "dense_equiv_tflops": 14.0 * d * float(Bn * H) * N * N * ws / (ms_step * 1e-3) / 1e12,
+            "roofline": roofline,
+            "roofline_all": roof,
+            "hybrid": hybrid,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(out))
+    if distributed:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="wan480", choices=("wan480", "wan720"))
+    ap.add_argument("--k-frac", type=float, default=None)
+    ap.add_argument("--p", type=float, default=0.0, help="Top-p of the headline step (0 = off)")
+    ap.add_argument("--no-hybrid", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from block_sparse_attention_sparge_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    k_frac = wl.k_frac if args.k_frac is None else args.k_frac
+    if args.impl == "reference":
+        return run_reference(args, wl, k_frac, args.p)
+    return run_ours(args, wl, k_frac, args.p)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -372,12 +372,13 @@ def _kept_tokens(cols: np.ndarray, n: int, bk: int) -> np.ndarray:
 
 
 def sparse_attention_blocks(q, k, v, block_mask, bq: int, bk: int, scale=None,
-                            dtype=np.float64, heads=None):
+                            dtype=np.float64, heads=None, qblocks=None):
     """Block-gather formulation of ``sparse_attention_dense`` (same definition):
     for each q-block gather the tokens of its kept kv-blocks and run a plain
     softmax attention over them.  Used for shapes too large for the dense
-    N x N form.  ``heads`` optionally restricts to a list of (b, h) pairs;
-    rows of other heads are left as NaN.  Returns (O, LSE) in ``dtype``."""
+    N x N form.  ``heads`` optionally restricts to a list of (b, h) pairs and
+    ``qblocks`` to a list of q-block indices; other rows are left as NaN.
+    Returns (O, LSE) in ``dtype``."""
     q = np.asarray(q)
     n, d = q.shape[-2], q.shape[-1]
     b_, h_ = q.shape[0], q.shape[1]
@@ -390,7 +391,7 @@ def sparse_attention_blocks(q, k, v, block_mask, bq: int, bk: int, scale=None,
         qh = np.asarray(q[b, h], dtype=dtype)
         kh = np.asarray(k[b, h], dtype=dtype)
         vh = np.asarray(v[b, h], dtype=dtype)
-        for i in range(mq):
+        for i in (range(mq) if qblocks is None else qblocks):
             lo, hi = i * bq, min(n, (i + 1) * bq)
             toks = _kept_tokens(np.nonzero(block_mask[b, h, i])[0], n, bk)
             if toks.size == 0:
@@ -407,10 +408,12 @@ def sparse_attention_blocks(q, k, v, block_mask, bq: int, bk: int, scale=None,
 
 
 def sparse_attention_blocks_bwd(q, k, v, dout, block_mask, bq: int, bk: int, scale=None,
-                                dtype=np.float64, heads=None):
+                                dtype=np.float64, heads=None, qblocks=None):
     """Block-gather form of ``sparse_attention_dense_bwd`` (same closed form),
     accumulating dK and dV over the q-blocks that keep each kv-block.
-    Returns (dQ, dK, dV); heads not listed in ``heads`` are NaN."""
+    Returns (dQ, dK, dV); heads not listed in ``heads`` are NaN.  With
+    ``qblocks`` only those q-blocks contribute (a partial sum, used to time
+    a bounded sample of the work)."""
     q = np.asarray(q)
     n, d = q.shape[-2], q.shape[-1]
     b_, h_ = q.shape[0], q.shape[1]
@@ -428,7 +431,7 @@ def sparse_attention_blocks_bwd(q, k, v, dout, block_mask, bq: int, bk: int, sca
         dkh = np.zeros_like(kh)
         dvh = np.zeros_like(vh)
         dqh = np.zeros_like(qh)
-        for i in range(mq):
+        for i in (range(mq) if qblocks is None else qblocks):
             lo, hi = i * bq, min(n, (i + 1) * bq)
             toks = _kept_tokens(np.nonzero(block_mask[b, h, i])[0], n, bk)
             if toks.size == 0:
