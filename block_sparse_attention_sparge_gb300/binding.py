@@ -74,6 +74,7 @@ _SIGNATURES = {
     "sparge_mask_workspace_bytes": ([_SHP, ctypes.POINTER(_SZ)], _I),
     "sparge_mask": ([_SHP, _P, _P, _F, _F, _F, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "sparge_mask_from_prob": ([_SHP, _P, _F, _F, _P, _P, _P, _P, _P, _P, _P], _I),
+    "sparge_mask_noalloc": ([_SHP, _P, _P, _F, _F, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "sparge_attn_fwd": ([_SHP, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P], _I),
     "sparge_attn_bwd_workspace_bytes": ([_SHP, ctypes.POINTER(_SZ)], _I),
     "sparge_attn_bwd": ([_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P, _SZ,

@@ -15,7 +15,8 @@
  *   Mk = ceil(N/block_kv).  The last block of each may be partial.
  * - The caller owns every buffer and the stream.  The library allocates,
  *   frees and synchronises nothing (sparge_read_status excepted, which
- *   synchronises the given stream), and keeps no global mutable state.
+ *   synchronises the given stream), and keeps no global mutable state apart
+ *   from the fixed scratch array of sparge_mask_noalloc.
  * - All launches are asynchronous on `stream` (NULL = the legacy default
  *   stream).  Arguments are validated before any launch; on an error nothing
  *   is launched and a negative status is returned.
@@ -110,6 +111,32 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
                 float softmax_scale, uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
                 int32_t* col_idx, int32_t* col_cnt, float* pooled_logit, float* pooled_prob,
                 void* workspace, size_t ws_bytes, int32_t* status, sparge_stream_t stream);
+
+/*
+ * sparge_mask_noalloc -- sparge_mask without a workspace argument, for
+ * callers that cannot allocate device memory (a runtime that owns all device
+ * memory through its own pool allocator; a latency-critical loop in which an
+ * allocation or free may synchronise the device).  The method pages have no
+ * counterpart of this call; it is a deployment variant of sparge_mask.
+ *   Same arguments, outputs and results as sparge_mask, minus workspace and
+ *   ws_bytes.  The pooled Q and K live in a fixed 8 MiB device array inside
+ *   the library, one per GPU that loads it, kept until the process exits.
+ *   Shapes whose workspace (sparge_mask_workspace_bytes) exceeds 8 MiB return
+ *   SPARGE_ERR_WORKSPACE before any launch.
+ *   The first call on a device (made with that device current) looks up the
+ *   array's device address once; make that first call before any stream
+ *   capture.  It allocates nothing: no cudaMalloc, cudaFree or allocating
+ *   library routine.
+ *   Every call on a device shares the one array, which keeps the last call's
+ *   contents (each call overwrites what it reads, so nothing needs clearing).
+ *   Calls that overlap on the GPU (different streams, or host threads on the
+ *   same device without ordering) race on the array: serialise them.
+ */
+int sparge_mask_noalloc(const sparge_shape* shape, const void* q, const void* k, float k_frac,
+                        float p, float softmax_scale, uint32_t* bitmask, int32_t* row_idx,
+                        int32_t* row_cnt, int32_t* col_idx, int32_t* col_cnt,
+                        float* pooled_logit, float* pooled_prob, int32_t* status,
+                        sparge_stream_t stream);
 
 /*
  * sparge_mask_from_prob -- step 3 alone: the hybrid selection of sparge_mask
