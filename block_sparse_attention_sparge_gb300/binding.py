@@ -81,6 +81,7 @@ _SIGNATURES = {
                          _P, _P], _I),
     "sparge_read_status": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], _I),
     "sparge_debug_wait_probe": ([_P, ctypes.c_uint64, _P], _I),
+    "sparge_debug_exp2_poly": ([_P, _P, _I, _P], _I),
 }
 
 _lib = None
@@ -280,6 +281,16 @@ def sparge_attn_bwd(q, k, v, o, lse, dout, row_idx, row_cnt, col_idx, col_cnt,
            "sparge_attn_bwd")
     _finish(st, check_status, "sparge_attn_bwd")
     return dq, dk, dv
+
+
+def sparge_debug_exp2_poly(x: torch.Tensor) -> torch.Tensor:
+    """2^x by the library's FMA-pipe polynomial (for testing it)."""
+    if not (x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous fp32 CUDA tensor")
+    y = torch.empty_like(x)
+    _check(load_library().sparge_debug_exp2_poly(_ptr(x), _ptr(y), x.numel(), _stream(x.device)),
+           "sparge_debug_exp2_poly")
+    return y
 
 
 def sparge_debug_wait_probe(timeout_ns: int = 10_000_000, device="cuda") -> int:

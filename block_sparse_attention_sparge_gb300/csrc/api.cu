@@ -92,7 +92,7 @@ size_t mask_ws_bytes(const Geom& g) {
          round_up((size_t)g.BH * g.d * g.Mk * sizeof(float));
 }
 
-size_t bwd_ws_bytes(const Geom& g) { return round_up((size_t)g.BH * g.N * sizeof(float)); }
+size_t bwd_ws_bytes(const Geom& g) { return bwd_workspace_bytes(g); }
 
 // ---------------------------------------------------------------- wait probe
 __global__ void wait_probe_kernel(int32_t* status, uint64_t timeout_ns) {
@@ -105,6 +105,11 @@ __global__ void wait_probe_kernel(int32_t* status, uint64_t timeout_ns) {
   __syncthreads();
   // Nothing arrives on `bar`: the bounded wait must give up and report.
   if (!mbar_wait(b, 0, timeout_ns)) report_error(status, SPARGE_ERR_TIMEOUT);
+}
+
+__global__ void exp2_poly_kernel(const float* __restrict__ x, float* __restrict__ y, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = exp2_poly(x[i]);
 }
 
 }  // namespace
@@ -259,8 +264,8 @@ int sparge_attn_bwd(const sparge_shape* shape, const void* q, const void* k, con
   if (workspace == nullptr || ws_bytes < bwd_ws_bytes(g)) return SPARGE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SPARGE_ERR_MISALIGNED;
   return cuda_status(launch_attn_bwd(g, q, k, v, o, lse, dout, row_idx, row_cnt, col_idx, col_cnt,
-                                     resolve_scale(softmax_scale, g.d), dq, dk, dv,
-                                     static_cast<float*>(workspace), status, stream));
+                                     resolve_scale(softmax_scale, g.d), dq, dk, dv, workspace,
+                                     status, stream));
 }
 
 int sparge_read_status(const int32_t* status, sparge_stream_t stream, int32_t* host_status) {
@@ -272,6 +277,15 @@ int sparge_read_status(const int32_t* status, sparge_stream_t stream, int32_t* h
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SPARGE_ERR_CUDA;
   *host_status = h;
   return SPARGE_OK;
+}
+
+int sparge_debug_exp2_poly(const float* x, float* y, int n, sparge_stream_t stream) {
+  SPARGE_TRY(check_word(x));
+  SPARGE_TRY(check_word(y));
+  if (n < 0) return SPARGE_ERR_INVALID_ARG;
+  if (n == 0) return SPARGE_OK;
+  exp2_poly_kernel<<<(n + 255) / 256, 256, 0, stream>>>(x, y, n);
+  return cuda_status(cudaGetLastError());
 }
 
 int sparge_debug_wait_probe(int32_t* status, uint64_t timeout_ns, sparge_stream_t stream) {

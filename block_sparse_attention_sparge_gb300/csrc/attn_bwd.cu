@@ -39,6 +39,9 @@ constexpr int kBM = 128;
 constexpr int kBN = 64;
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
+#ifndef SPARGE_BWD_POLY_EVERY
+#define SPARGE_BWD_POLY_EVERY 0
+#endif
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 template <int D>
@@ -66,6 +69,67 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 #pragma unroll
   for (int off = CH / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (c == 0 && r < rows) delta[r] = s;
+}
+
+// ---------------------------------------------------------------- work order
+// Longest-first launch order: writes order[pos] = item for items [0, n) sorted
+// by count descending (a counting sort; equal counts in any order).  Launching
+// the longest lists first keeps a few long lists (attention-sink blocks that
+// every q-block keeps) from running alone at the end of the grid.
+constexpr int kOrderThreads = 1024;
+__global__ void __launch_bounds__(kOrderThreads) order_by_count_kernel(
+    const int32_t* __restrict__ cnt, int n, int max_cnt, int32_t* __restrict__ order) {
+  extern __shared__ int32_t start[];  // [max_cnt + 1], indexed by count
+  __shared__ int32_t warp_tot[kOrderThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int nb = max_cnt + 1;
+  for (int b = tid; b < nb; b += kOrderThreads) start[b] = 0;
+  __syncthreads();
+  for (int it = tid; it < n; it += kOrderThreads)
+    atomicAdd(&start[min(max(__ldg(cnt + it), 0), max_cnt)], 1);
+  __syncthreads();
+  // Exclusive scan over counts in descending order: thread t owns the run of
+  // E reversed positions [t*E, t*E + E), position r meaning count max_cnt - r.
+  const int E = (nb + kOrderThreads - 1) / kOrderThreads;
+  int local = 0;
+  for (int e = 0; e < E; ++e) {
+    const int r = tid * E + e;
+    if (r < nb) local += start[max_cnt - r];
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += v;
+    }
+    warp_tot[lane] = t;  // inclusive warp totals
+  }
+  __syncthreads();
+  int run = incl - local + (w > 0 ? warp_tot[w - 1] : 0);
+  __syncthreads();  // every thread has read its histogram run
+  for (int e = 0; e < E; ++e) {
+    const int r = tid * E + e;
+    if (r < nb) {
+      const int c = max_cnt - r;
+      const int h = start[c];
+      start[c] = run;
+      run += h;
+    }
+  }
+  __syncthreads();
+  for (int it = tid; it < n; it += kOrderThreads) {
+    const int pos = atomicAdd(&start[min(max(__ldg(cnt + it), 0), max_cnt)], 1);
+    order[pos] = it;
+  }
 }
 
 // Loads 64 fp32 columns of one TMEM lane (4 x 16) starting at `addr`.
@@ -113,16 +177,16 @@ struct DkdvCfg {
   static constexpr uint32_t off_v = off_k + kKV;
   static constexpr uint32_t off_q = off_v + kKV;                 // NST stages of Q
   static constexpr uint32_t off_do = off_q + NST * kQ;           // NST stages of dO
-  static constexpr uint32_t off_p = off_do + NST * kQ;
-  static constexpr uint32_t off_ds = off_p + kP;
-  static constexpr uint32_t off_bar = off_ds + kP;
+  static constexpr uint32_t off_p = off_do + NST * kQ;    // 2 buffers
+  static constexpr uint32_t off_ds = off_p + 2 * kP;      // 2 buffers
+  static constexpr uint32_t off_bar = off_ds + 2 * kP;
   static constexpr int B_KV = 0;
   static constexpr int B_QF = 1;
   static constexpr int B_QE = B_QF + NST;
   static constexpr int B_SF = B_QE + NST;  // 2
-  static constexpr int B_PSF = B_SF + 2;   // count 128
-  static constexpr int B_PSE = B_PSF + 1;
-  static constexpr int B_DONE = B_PSE + 1;
+  static constexpr int B_PSF = B_SF + 2;   // 2, count 128
+  static constexpr int B_PSE = B_PSF + 2;  // 2
+  static constexpr int B_DONE = B_PSE + 2;
   static constexpr int NBAR = B_DONE + 1;
   static constexpr uint32_t off_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_slot + 16;
@@ -137,8 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const float* __restrict__ lse, const float* __restrict__ delta,
-                    const int32_t* __restrict__ col_idx, const int32_t* __restrict__ col_cnt, int N,
-                    int Mq, int Mk, float scale, float scale_log2, __nv_bfloat16* __restrict__ dk,
+                    const int32_t* __restrict__ col_idx, const int32_t* __restrict__ col_cnt,
+                    const int32_t* __restrict__ col_order, int N, int Mq, int Mk, float scale,
+                    float scale_log2, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, int32_t* __restrict__ status) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -149,15 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / Mk;
-  const int j = blockIdx.x % Mk;
+  const int item = min(max(__ldg(col_order + blockIdx.x), 0), static_cast<int>(gridDim.x) - 1);
+  const int bh = item / Mk;
+  const int j = item % Mk;
   const long long col_id = (long long)bh * Mk + j;
   const int n = min(max(__ldg(col_cnt + col_id), 0), Mq);
   const int32_t* list = col_idx + col_id * Mq;
   const int kv_valid = min(kBN, N - j * kBN);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i) mbar_init(bar(i), i == C::B_PSF ? 128u : 1u);
+    for (int i = 0; i < C::NBAR; ++i)
+      mbar_init(bar(i), (i == C::B_PSF || i == C::B_PSF + 1) ? 128u : 1u);
     fence_barrier_init();
   }
   if (warp == 5) {
@@ -231,29 +298,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t >= 1) {
           const int u = t - 1;
           const int su = u % C::NST;
-          if (!mbar_wait(bar(C::B_PSF), u & 1, kWaitTimeoutNs)) {
+          const int pb = u & 1;
+          if (!mbar_wait(bar(C::B_PSF + pb), (u >> 1) & 1, kWaitTimeoutNs)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t qb = s0 + C::off_q + su * C::kQ;
           const uint32_t ob = s0 + C::off_do + su * C::kQ;
+          const uint32_t pbuf = s0 + C::off_p + pb * C::kP;
+          const uint32_t dsbuf = s0 + C::off_ds + pb * C::kP;
 #pragma unroll
           for (int kk = 0; kk < kBM / 16; ++kk) {
             // A = dO^T (M = d, MN-major: 64-element chunks kBM*128 apart),
             // B = P (N = kv, MN-major); K = 16 query rows per step.
             tc_mma_bf16(tmem + C::col_dv, sdesc_sw128(ob + kk * 2048, kBM * 128, 1024),
-                        sdesc_sw128(s0 + C::off_p + kk * 2048, kBM * 128, 1024), idG,
+                        sdesc_sw128(pbuf + kk * 2048, kBM * 128, 1024), idG,
                         (u > 0 || kk > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < kBM / 16; ++kk) {
             tc_mma_bf16(tmem + C::col_dk, sdesc_sw128(qb + kk * 2048, kBM * 128, 1024),
-                        sdesc_sw128(s0 + C::off_ds + kk * 2048, kBM * 128, 1024), idG,
+                        sdesc_sw128(dsbuf + kk * 2048, kBM * 128, 1024), idG,
                         (u > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bar(C::B_QE + su));
-          tc_commit(bar(C::B_PSE));
+          tc_commit(bar(C::B_PSE + pb));
         }
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
@@ -264,12 +334,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     bool ok = true;
+    // Two-deep prefetch: the q-block index of tile t+2 and the LSE / D of
+    // tile t+1 are loaded while tile t is computed.
+    const float* lse_h = lse + (long long)bh * N;
+    const float* del_h = delta + (long long)bh * N;
+    auto row_of = [&](int qi) { return qi * kBM + r; };
+    int i_n1 = n > 0 ? min(max(__ldg(list), 0), Mq - 1) : 0;
+    int i_n2 = n > 1 ? min(max(__ldg(list + 1), 0), Mq - 1) : 0;
+    float lse_n = 0.f, del_n = 0.f;
+    if (n > 0 && row_of(i_n1) < N) {
+      lse_n = __ldg(lse_h + row_of(i_n1));
+      del_n = __ldg(del_h + row_of(i_n1));
+    }
     for (int t = 0; t < n; ++t) {
-      const int i = min(max(__ldg(list + t), 0), Mq - 1);
-      const int row = i * kBM + r;
-      const bool rv = row < N;
-      const float lse2 = rv ? __ldg(lse + (long long)bh * N + row) * kLog2e : 0.f;
-      const float drow = rv ? __ldg(delta + (long long)bh * N + row) : 0.f;
+      const bool rv = row_of(i_n1) < N;
+      const float lse2 = rv ? lse_n * kLog2e : 0.f;
+      const float drow = rv ? del_n : 0.f;
+      i_n1 = i_n2;
+      if (t + 1 < n && row_of(i_n1) < N) {
+        lse_n = __ldg(lse_h + row_of(i_n1));
+        del_n = __ldg(del_h + row_of(i_n1));
+      }
+      if (t + 2 < n) i_n2 = min(max(__ldg(list + t + 2), 0), Mq - 1);
       if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
         ok = false;
         break;
@@ -282,29 +368,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld64(lane_base + (t & 1) * 128 + 64, dp);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          float p0 = exp2f(fmaf(s[c], scale_log2, -lse2));
-          float p1 = exp2f(fmaf(s[c + 1], scale_log2, -lse2));
+          float p0 = exp2_split<SPARGE_BWD_POLY_EVERY>(c, fmaf(s[c], scale_log2, -lse2));
+          float p1 = exp2_split<SPARGE_BWD_POLY_EVERY>(c + 1, fmaf(s[c + 1], scale_log2, -lse2));
           if (!rv || c >= kv_valid) p0 = 0.f;
           if (!rv || c + 1 >= kv_valid) p1 = 0.f;
           pk[c / 2] = pack_bf16x2(p0, p1);
           dk_[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
         }
       }
-      if (t >= 1 && !warp_wait(bar(C::B_PSE), (t - 1) & 1)) {
+      // Buffer t & 1 is free once the dV/dK MMAs of tile t-2 have completed.
+      if (t >= 2 && !warp_wait(bar(C::B_PSE + (t & 1)), ((t - 2) >> 1) & 1)) {
         ok = false;
         break;
       }
-      store_row_sw128(sm + C::off_p, r, pk);
-      store_row_sw128(sm + C::off_ds, r, dk_);
+      store_row_sw128(sm + C::off_p + (t & 1) * C::kP, r, pk);
+      store_row_sw128(sm + C::off_ds + (t & 1) * C::kP, r, dk_);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(C::B_PSF));
+      mbar_arrive(bar(C::B_PSF + (t & 1)));
     }
     if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
     // Epilogue: thread r holds column r of dV^T / dK^T (= feature r of 64 kv rows).
     bool have = ok && n > 0;
     if (have) {
-      have = warp_wait(bar(C::B_PSE), (n - 1) & 1);
+      have = warp_wait(bar(C::B_PSE + ((n - 1) & 1)), ((n - 1) >> 1) & 1);
       if (!have) report_error(status, SPARGE_ERR_TIMEOUT);
     }
     tc_fence_after();
@@ -377,9 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const float* __restrict__ lse, const float* __restrict__ delta,
-                  const int32_t* __restrict__ row_idx, const int32_t* __restrict__ row_cnt, int N,
-                  int Mq, int Mk, float scale, float scale_log2, __nv_bfloat16* __restrict__ dq,
-                  int32_t* __restrict__ status) {
+                  const int32_t* __restrict__ row_idx, const int32_t* __restrict__ row_cnt,
+                  const int32_t* __restrict__ row_order, int N, int Mq, int Mk, float scale,
+                  float scale_log2, __nv_bfloat16* __restrict__ dq, int32_t* __restrict__ status) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -389,8 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / Mq;
-  const int qb = blockIdx.x % Mq;
+  const int item = min(max(__ldg(row_order + blockIdx.x), 0), static_cast<int>(gridDim.x) - 1);
+  const int bh = item / Mq;
+  const int qb = item % Mq;
   const long long row_id = (long long)bh * Mq + qb;
   const int n = min(max(__ldg(row_cnt + row_id), 0), Mk);
   const int32_t* list = row_idx + row_id * Mk;
@@ -507,8 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = (rv && n > 0) ? __ldg(lse + (long long)bh * N + row) * kLog2e : 0.f;
     const float drow = rv ? __ldg(delta + (long long)bh * N + row) : 0.f;
     bool ok = true;
+    int j_next = n > 0 ? min(max(__ldg(list), 0), Mk - 1) : 0;  // one tile ahead
     for (int t = 0; t < n; ++t) {
-      const int jj = min(max(__ldg(list + t), 0), Mk - 1);
+      const int jj = j_next;
+      if (t + 1 < n) j_next = min(max(__ldg(list + t + 1), 0), Mk - 1);
       const int kv_valid = N - jj * kBN;
       if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
         ok = false;
@@ -522,8 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld64(lane_base + (t & 1) * 128 + 64, dp);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          float p0 = exp2f(fmaf(s[c], scale_log2, -lse2));
-          float p1 = exp2f(fmaf(s[c + 1], scale_log2, -lse2));
+          float p0 = exp2_split<SPARGE_BWD_POLY_EVERY>(c, fmaf(s[c], scale_log2, -lse2));
+          float p1 = exp2_split<SPARGE_BWD_POLY_EVERY>(c + 1, fmaf(s[c + 1], scale_log2, -lse2));
           if (!rv || c >= kv_valid) p0 = 0.f;
           if (!rv || c + 1 >= kv_valid) p1 = 0.f;
           pk[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
@@ -585,7 +675,9 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
                             const void* o, const float* lse, const void* dout,
                             const int32_t* row_idx, const int32_t* row_cnt,
                             const int32_t* col_idx, const int32_t* col_cnt, float scale, void* dq,
-                            void* dk, void* dv, float* delta, int32_t* status, cudaStream_t st) {
+                            void* dk, void* dv, void* workspace, int32_t* status, cudaStream_t st) {
+  const BwdWorkspace ws = bwd_workspace_layout(g, workspace);
+  float* delta = ws.delta;
   const long long rows = (long long)g.BH * g.N;
   constexpr int RPB = 256 / (D / 8);
   bwd_delta_kernel<D><<<static_cast<unsigned>((rows + RPB - 1) / RPB), 256, 0, st>>>(
@@ -600,12 +692,21 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
     return cudaErrorInvalidValue;
   const float scale_log2 = scale * kLog2e;
 
+  // Longest lists first: kv-blocks by CSC count, q-blocks by CSR count.
+  order_by_count_kernel<<<1, kOrderThreads, (g.Mq + 1) * sizeof(int32_t), st>>>(
+      col_cnt, g.BH * g.Mk, g.Mq, ws.col_order);
+  order_by_count_kernel<<<1, kOrderThreads, (g.Mk + 1) * sizeof(int32_t), st>>>(
+      row_cnt, g.BH * g.Mq, g.Mk, ws.row_order);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
   e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DkdvCfg<D>::smem_alloc);
   if (e != cudaSuccess) return e;
   bwd_dkdv_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mk), kThreads,
                        DkdvCfg<D>::smem_alloc, st>>>(
-      tq, tk, tv, tdo, lse, delta, col_idx, col_cnt, g.N, g.Mq, g.Mk, scale, scale_log2,
+      tq, tk, tv, tdo, lse, delta, col_idx, col_cnt, ws.col_order, g.N, g.Mq, g.Mk, scale,
+      scale_log2,
       static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -614,8 +715,8 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
                            DqCfg<D>::smem_alloc);
   if (e != cudaSuccess) return e;
   bwd_dq_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mq), kThreads, DqCfg<D>::smem_alloc,
-                     st>>>(tq, tk, tv, tdo, lse, delta, row_idx, row_cnt, g.N, g.Mq, g.Mk, scale,
-                           scale_log2, static_cast<__nv_bfloat16*>(dq), status);
+                     st>>>(tq, tk, tv, tdo, lse, delta, row_idx, row_cnt, ws.row_order, g.N, g.Mq,
+                           g.Mk, scale, scale_log2, static_cast<__nv_bfloat16*>(dq), status);
   return cudaGetLastError();
 }
 
@@ -625,12 +726,33 @@ cudaError_t launch_attn_bwd(const Geom& g, const void* q, const void* k, const v
                             const void* o, const float* lse, const void* dout,
                             const int32_t* row_idx, const int32_t* row_cnt,
                             const int32_t* col_idx, const int32_t* col_cnt, float scale, void* dq,
-                            void* dk, void* dv, float* delta, int32_t* status, cudaStream_t st) {
+                            void* dk, void* dv, void* workspace, int32_t* status, cudaStream_t st) {
   if (g.d == 128)
     return launch_bwd_impl<128>(g, q, k, v, o, lse, dout, row_idx, row_cnt, col_idx, col_cnt,
-                                scale, dq, dk, dv, delta, status, st);
+                                scale, dq, dk, dv, workspace, status, st);
   return launch_bwd_impl<64>(g, q, k, v, o, lse, dout, row_idx, row_cnt, col_idx, col_cnt, scale,
-                             dq, dk, dv, delta, status, st);
+                             dq, dk, dv, workspace, status, st);
+}
+
+namespace {
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+size_t bwd_workspace_bytes(const Geom& g) {
+  return align256((size_t)g.BH * g.N * sizeof(float)) +
+         align256((size_t)g.BH * g.Mk * sizeof(int32_t)) +
+         align256((size_t)g.BH * g.Mq * sizeof(int32_t));
+}
+
+BwdWorkspace bwd_workspace_layout(const Geom& g, void* base) {
+  uint8_t* p = static_cast<uint8_t*>(base);
+  BwdWorkspace w;
+  w.delta = reinterpret_cast<float*>(p);
+  p += align256((size_t)g.BH * g.N * sizeof(float));
+  w.col_order = reinterpret_cast<int32_t*>(p);
+  p += align256((size_t)g.BH * g.Mk * sizeof(int32_t));
+  w.row_order = reinterpret_cast<int32_t*>(p);
+  return w;
 }
 
 }  // namespace sparge

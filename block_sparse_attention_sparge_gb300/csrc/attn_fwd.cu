@@ -8,20 +8,25 @@
 // its q-block's kept kv-blocks only.
 //
 // One CTA computes one 128-token q-block of one head, looping over its CSR
-// list of kept 64-token kv-blocks:
-//   warp 4 (lane 0)  TMA producer: Q once, then K_j / V_j into a ring of stages.
-//   warp 5 (lane 0)  MMA issuer:   S_t = Q K_t^T into a double-buffered TMEM
-//                    tile (128 x 64 fp32), and O += P_t V_t into a TMEM
-//                    accumulator (128 x d fp32).  S_{t+1} is issued before
-//                    waiting for P_t so the tensor core overlaps the softmax.
-//   warps 0-3        softmax: thread r owns query row r (= TMEM lane r).  It
-//                    reads S_t, masks the ragged kv tail, keeps the running
-//                    max m and sum l in base 2, writes P_t (bf16) into shared
-//                    memory in the 128-byte-swizzled K-major layout the MMA
-//                    reads, and finally scales O by 1/l.  O is rescaled in
-//                    TMEM only when the running max grows by more than 8 (a
-//                    factor 256); below that the stale max stays exact
-//                    because the same max is used for l and for O.
+// list of kept 64-token kv-blocks; two CTAs share an SM so that one CTA's
+// latencies (barrier hand-offs, loads, its prologue and epilogue) overlap the
+// other's work.  Warp roles (224 threads):
+//   warp 4   TMA producer: Q once, then K_j / V_j into a 2-stage ring.
+//   warp 5   S issuer: S_t = Q K_t^T into a double-buffered TMEM tile
+//            (128 x 64 fp32).
+//   warp 6   PV issuer: O += P_t V_t into a TMEM accumulator (128 x d fp32).
+//            Separate issuing warps let the S and PV MMAs of neighbouring
+//            tiles overlap (a 128 x 64 x 16 MMA occupies the tensor pipe for
+//            about 48 cycles on this GPU).
+//   warps 0-3 softmax: thread r owns query row r (= TMEM lane r).  It reads
+//            S_t, masks the ragged kv tail, keeps the running max m and sum l
+//            in base 2 and writes P_t (bf16) into shared memory in the
+//            128-byte-swizzled K-major layout the PV MMA reads.  With d = 128
+//            P_t goes into the K half of tile t's own stage: K_t is dead once
+//            S_t has completed, and the stage is not reloaded before PV_t
+//            completes.  O is rescaled in TMEM only when the running max
+//            grows by more than 8 (a factor 256); below that the stale max
+//            stays exact because l and O share it.  Finally O is scaled by 1/l.
 // Every barrier wait is bounded; a timeout records SPARGE_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -36,33 +41,40 @@ namespace sparge {
 
 namespace {
 
-constexpr int kBM = 128;         // q-block rows
-constexpr int kBN = 64;          // kv-block rows
-constexpr int kFwdThreads = 192; // 4 softmax warps + producer + MMA
+constexpr int kBM = 128;           // q-block rows
+constexpr int kBN = 64;            // kv-block rows
+constexpr int kSoftmaxWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kSWarp = 5;
+constexpr int kPVWarp = 6;
+constexpr int kFwdThreads = 224;
+constexpr int kFwdCtasPerSm = 2;
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct FwdCfg {
-  static constexpr int NST = 3;                       // K/V stages
-  static constexpr int NP = 2;                        // P buffers
+  static constexpr int NST = 2;                       // K/V stages
+  static constexpr int NP = 2;                        // P phases (buffers when separate)
   static constexpr int KCH = D / 64;                  // 128-byte chunks per row
   static constexpr uint32_t kQ = kBM * D * 2;
   static constexpr uint32_t kKV = kBN * D * 2;
   static constexpr uint32_t kP = kBM * kBN * 2;
+  // P_t lives in tile t's K stage when that stage is large enough (d = 128).
+  static constexpr bool P_IN_K = kKV >= kP;
   static constexpr uint32_t off_q = 0;
   static constexpr uint32_t off_k = off_q + kQ;
   static constexpr uint32_t off_v = off_k + NST * kKV;
   static constexpr uint32_t off_p = off_v + NST * kKV;
-  static constexpr uint32_t off_bar = off_p + NP * kP;
+  static constexpr uint32_t off_bar = off_p + (P_IN_K ? 0 : NP * kP);
   // barriers
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;
   static constexpr int B_VF = B_KF + NST;
   static constexpr int B_KE = B_VF + NST;
   static constexpr int B_SF = B_KE + NST;
-  static constexpr int B_PF = B_SF + 2;
+  static constexpr int B_PF = B_SF + 2;     // count 128 (all softmax threads)
   static constexpr int B_PV = B_PF + NP;
-  static constexpr int B_DRAIN = B_PV + 2;
+  static constexpr int B_DRAIN = B_PV + 2;  // count 2 (both issuers)
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t off_tmem_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_tmem_slot + 16;
@@ -72,8 +84,15 @@ struct FwdCfg {
   static constexpr uint32_t col_o = 128;
 };
 
+// Shared-memory address of P_t.
 template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__device__ __forceinline__ uint32_t p_tile_addr(uint32_t s0, int t) {
+  using C = FwdCfg<D>;
+  return C::P_IN_K ? s0 + C::off_k + (t % C::NST) * C::kKV : s0 + C::off_p + (t % C::NP) * C::kP;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ row_idx,
                     const int32_t* __restrict__ row_cnt, int N, int Mq, int Mk, float scale_log2,
@@ -96,11 +115,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int32_t* list = row_idx + row_id * Mk;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i)
-      mbar_init(bar(i), (i >= C::B_PF && i < C::B_PF + C::NP) ? 128u : 1u);
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i >= C::B_PF && i < C::B_PF + C::NP) cnt = 32 * kSoftmaxWarps;
+      if (i == C::B_DRAIN) cnt = 2;
+      mbar_init(bar(i), cnt);
+    }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kSWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::tmem_cols);
     tmem_relinquish();
   }
@@ -109,7 +132,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tmQ);
@@ -143,55 +166,65 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs);
       }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kSWarp) {
+    // ------------------------------------------------------------ S issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
       bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
-      for (int t = 0; ok && t <= n; ++t) {
-        if (t < n) {
-          const int s = t % C::NST;
-          if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kbase = s0 + C::off_k + s * C::kKV;
-          const uint32_t dS = tmem + C::col_s + (t & 1) * kBN;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk & 3) * 32;
-            const uint64_t a = sdesc_sw128(s0 + C::off_q + (kk >> 2) * (kBM * 128) + koff, 16, 1024);
-            const uint64_t b = sdesc_sw128(kbase + (kk >> 2) * (kBN * 128) + koff, 16, 1024);
-            tc_mma_bf16(dS, a, b, idS, kk > 0);
-          }
-          tc_commit(bar(C::B_SF + (t & 1)));
+      for (int t = 0; ok && t < n; ++t) {
+        const int s = t % C::NST;
+        // S buffer t & 1 was last read by the softmax of tile t - 2, which
+        // finished reading it before P(t - 2) became full.
+        if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs) ||
+            (t >= 2 &&
+             !mbar_wait(bar(C::B_PF + (t % C::NP)), ((t - 2) / C::NP) & 1, kWaitTimeoutNs))) {
+          ok = false;
+          break;
         }
-        if (t >= 1) {
-          const int u = t - 1;
-          const int su = u % C::NST;
-          const int pb = u % C::NP;
-          if (!mbar_wait(bar(C::B_PF + pb), (u / C::NP) & 1, kWaitTimeoutNs) ||
-              !mbar_wait(bar(C::B_VF + su), (u / C::NST) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t pbase = s0 + C::off_p + pb * C::kP;
-          const uint32_t vbase = s0 + C::off_v + su * C::kKV;
+        tc_fence_after();
+        const uint32_t kbase = s0 + C::off_k + s * C::kKV;
+        const uint32_t dS = tmem + C::col_s + (t & 1) * kBN;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(pbase + kk * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024);
-            tc_mma_bf16(tmem + C::col_o, a, b, idO, (u > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(bar(C::B_KE + su));
-          tc_commit(bar(C::B_PV + (u & 1)));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(s0 + C::off_q + (kk >> 2) * (kBM * 128) + koff, 16, 1024);
+          const uint64_t b = sdesc_sw128(kbase + (kk >> 2) * (kBN * 128) + koff, 16, 1024);
+          tc_mma_bf16(dS, a, b, idS, kk > 0);
         }
+        tc_commit(bar(C::B_SF + (t & 1)));
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      // Drain: every MMA issued above has completed once this arrives.
+      // Drain: every MMA this thread issued has completed once this arrives.
+      tc_commit(bar(C::B_DRAIN));
+      mbar_wait(bar(C::B_DRAIN), 0, kWaitTimeoutNs);
+    }
+  } else if (warp == kPVWarp) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
+      bool ok = true;
+      for (int u = 0; ok && u < n; ++u) {
+        const int su = u % C::NST;
+        if (!mbar_wait(bar(C::B_PF + (u % C::NP)), (u / C::NP) & 1, kWaitTimeoutNs) ||
+            !mbar_wait(bar(C::B_VF + su), (u / C::NST) & 1, kWaitTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t pbase = p_tile_addr<D>(s0, u);
+        const uint32_t vbase = s0 + C::off_v + su * C::kKV;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(pbase + kk * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024);
+          tc_mma_bf16(tmem + C::col_o, a, b, idO, (u > 0 || kk > 0) ? 1u : 0u);
+        }
+        // S(u) completed before P(u) was written, so stage su (K and V) is free
+        // once this PV completes.
+        tc_commit(bar(C::B_KE + su));
+        tc_commit(bar(C::B_PV + (u & 1)));
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DRAIN));
       mbar_wait(bar(C::B_DRAIN), 0, kWaitTimeoutNs);
     }
@@ -203,7 +236,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    // Scores are kept raw; the scale folds into one FFMA before the exp.  The
+    // row max is taken on raw scores (the min when the scale is negative).
+    const bool pos = scale_log2 > 0.f;
+    const float masked = pos ? -INFINITY : INFINITY;
+    // The kv-block index of the next tile is loaded one tile ahead.
+    int j_next = n > 0 ? min(max(__ldg(list), 0), Mk - 1) : 0;
     for (int t = 0; t < n; ++t) {
+      const int j = j_next;
+      if (t + 1 < n) j_next = min(max(__ldg(list + t + 1), 0), Mk - 1);
       if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
         ok = false;
         break;
@@ -223,22 +264,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         SPARGE_TMEM_WAIT_LD16(rd);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          x[c] = __uint_as_float(ra[c]) * scale_log2;
-          x[16 + c] = __uint_as_float(rb[c]) * scale_log2;
-          x[32 + c] = __uint_as_float(rc[c]) * scale_log2;
-          x[48 + c] = __uint_as_float(rd[c]) * scale_log2;
+          x[c] = __uint_as_float(ra[c]);
+          x[16 + c] = __uint_as_float(rb[c]);
+          x[32 + c] = __uint_as_float(rc[c]);
+          x[48 + c] = __uint_as_float(rd[c]);
         }
       }
-      const int j = min(max(__ldg(list + t), 0), Mk - 1);
       const int valid = N - j * kBN;
       if (valid < kBN) {
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
-          if (c >= valid) x[c] = -INFINITY;
+          if (c >= valid) x[c] = masked;
       }
-      float mt = x[0];
+      // Row max as a tree over 8 independent partial maxima.
+      float mp[8];
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mt = fmaxf(mt, x[c]);
+      for (int e = 0; e < 8; ++e) mp[e] = x[e];
+      if (pos) {
+#pragma unroll
+        for (int c = 8; c < kBN; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+        mp[0] = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                      fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      } else {
+#pragma unroll
+        for (int c = 8; c < kBN; ++c) mp[c & 7] = fminf(mp[c & 7], x[c]);
+        mp[0] = fminf(fminf(fminf(mp[0], mp[1]), fminf(mp[2], mp[3])),
+                      fminf(fminf(mp[4], mp[5]), fminf(mp[6], mp[7])));
+      }
+      const float mt = mp[0] * scale_log2;
       const float m_new = fmaxf(m_used, mt);
       // Rescale decision must be warp-uniform (tcgen05.ld/st are warp-wide).
       const bool want = (t > 0) && (m_new - m_used > kRescaleLog2);
@@ -266,23 +319,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           m_used = m_new;
         }
       }
-      // P buffer t % NP is free once PV(t - NP) has completed.
-      if (t >= C::NP) {
+      // A separate P buffer t % NP is free once PV(t - NP) has completed; P in
+      // the K stage needs no wait (the stage held K_t, already consumed).
+      if (!C::P_IN_K && t >= C::NP) {
         const int u = t - C::NP;
         if (!warp_wait(bar(C::B_PV + (u & 1)), (u >> 1) & 1)) {
           ok = false;
           break;
         }
       }
-      uint8_t* prow = sm + C::off_p + (t % C::NP) * C::kP;
-      float rs = 0.f;
+      uint8_t* prow = sm + (p_tile_addr<D>(s0, t) - s0);
+      float rs8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          p[e] = exp2f(x[ch * 8 + e] - m_used);
-          rs += p[e];
+          p[e] = ex2_approx(fmaf(x[ch * 8 + e], scale_log2, -m_used));
+          rs8[e] += p[e];
         }
         uint4 v;
         v.x = pack_bf16x2(p[0], p[1]);
@@ -291,7 +347,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         v.w = pack_bf16x2(p[6], p[7]);
         *reinterpret_cast<uint4*>(prow + sw128_offset(r, ch * 16)) = v;
       }
-      l += rs;
+      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_PF + (t % C::NP)));
@@ -301,7 +357,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const bool have = ok && n > 0 && warp_wait(bar(C::B_PV + ((n - 1) & 1)), ((n - 1) >> 1) & 1);
     if (ok && n > 0 && !have) report_error(status, SPARGE_ERR_TIMEOUT);
     tc_fence_after();
-    const float inv_l = (have && l > 0.f) ? 1.f / l : 0.f;
+    const bool good = have && l > 0.f;
+    const float inv_l = good ? 1.f / l : 0.f;
     __nv_bfloat16* orow = out + ((long long)bh * N + row) * D;
     const bool in_range = row < N;
 #pragma unroll 1
@@ -330,12 +387,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     if (lse != nullptr && in_range)
       lse[(long long)bh * N + row] =
-          (have && l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+          good ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kSWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::tmem_cols);
   }

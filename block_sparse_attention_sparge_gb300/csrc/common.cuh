@@ -209,6 +209,36 @@ SPARGE_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 2^x by the hardware approximation (MUFU.EX2), subnormal results flushed.
+SPARGE_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^x on the FMA pipe, to take load off the special-function unit.  Split
+// x = i + f with i = floor(x) and f in [0, 1); 2^f is a cubic whose
+// coefficients were fitted here by weighted least squares on [0, 1) (max
+// relative error 8.6e-5, far below bf16 resolution), and 2^i is added to the
+// exponent field.  Results below 2^-126 (and x = -inf) flush to 0.
+SPARGE_DEV float exp2_poly(float x) {
+  const float xc = fmaxf(x, -126.f);
+  const float fi = floorf(xc);
+  const float f = xc - fi;
+  const float p = fmaf(fmaf(fmaf(0.07706708f, f, 0.22764495f), f, 0.6951168f), f, 1.0f);
+  const float r = __int_as_float(__float_as_int(p) + (static_cast<int>(fi) << 23));
+  return x < -126.f ? 0.f : r;
+}
+
+// Columns c of a 64-wide score row whose exp2 runs on the FMA pipe: every
+// kPolyEvery-th column (0 = none).  Tuned per kernel by measurement.
+template <int kPolyEvery>
+SPARGE_DEV float exp2_split(int c, float x) {
+  if (kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == (kPolyEvery > 0 ? kPolyEvery - 1 : 0))
+    return exp2_poly(x);
+  return ex2_approx(x);
+}
+
 SPARGE_DEV uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
 }  // namespace sparge

@@ -38,12 +38,20 @@ cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const v
                             const int32_t* row_idx, const int32_t* row_cnt, float scale, void* o,
                             float* lse, int32_t* status, cudaStream_t st);
 
-// attn_bwd.cu
+// attn_bwd.cu.  Workspace: D = rowsum(dO*O) fp32 [BH, N], then the
+// longest-first launch orders of kv-blocks [BH*Mk] and q-blocks [BH*Mq].
+struct BwdWorkspace {
+  float* delta;
+  int32_t* col_order;
+  int32_t* row_order;
+};
+size_t bwd_workspace_bytes(const Geom& g);
+BwdWorkspace bwd_workspace_layout(const Geom& g, void* base);
 cudaError_t launch_attn_bwd(const Geom& g, const void* q, const void* k, const void* v,
                             const void* o, const float* lse, const void* dout,
                             const int32_t* row_idx, const int32_t* row_cnt,
                             const int32_t* col_idx, const int32_t* col_cnt, float scale, void* dq,
-                            void* dk, void* dv, float* delta, int32_t* status, cudaStream_t st);
+                            void* dk, void* dv, void* workspace, int32_t* status, cudaStream_t st);
 
 // api.cu
 cudaError_t launch_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t st);

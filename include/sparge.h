@@ -170,7 +170,8 @@ int sparge_attn_fwd(const sparge_shape* shape, const void* q, const void* k, con
                     const int32_t* row_idx, const int32_t* row_cnt, float softmax_scale,
                     void* o, float* lse, int32_t* status, sparge_stream_t stream);
 
-/* Workspace bytes sparge_attn_bwd needs (fp32 D = rowsum(dO*O) per token). */
+/* Workspace bytes sparge_attn_bwd needs: fp32 D = rowsum(dO*O) per token and
+ * the longest-first launch orders of kv-blocks and q-blocks (int32). */
 int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
 
 /*
@@ -205,6 +206,14 @@ int sparge_read_status(const int32_t* status, sparge_stream_t stream, int32_t* h
  * path that never hangs the GPU.
  */
 int sparge_debug_wait_probe(int32_t* status, uint64_t timeout_ns, sparge_stream_t stream);
+
+/*
+ * sparge_debug_exp2_poly -- y[i] = 2^x[i] by the FMA-pipe polynomial the
+ * attention kernels can use for part of their exponentials (x = i + f,
+ * fitted cubic for 2^f, relative error < 1e-4; values below 2^-126 flush to
+ * 0).  For testing that routine against CUDA's exp2.  x, y: fp32 device, n >= 0.
+ */
+int sparge_debug_exp2_poly(const float* x, float* y, int n, sparge_stream_t stream);
 
 #ifdef __cplusplus
 }
