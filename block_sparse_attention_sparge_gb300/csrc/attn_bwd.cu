@@ -20,8 +20,9 @@
 //   bwd_dq_kernel     one CTA per q-block, loops over its kept kv-blocks (CSR
 //                     list); recomputes S, dP and dS and accumulates
 //                     dQ += dS K in TMEM.
-// Roles per CTA: warps 0-3 compute (thread r = TMEM lane r), warp 4 TMA
-// producer, warp 5 MMA issuer.  Every wait is bounded.
+// Roles per CTA: eight compute warps (two per TMEM lane quarter, each owning
+// 32 of a tile's 64 key columns), a TMA producer warp and two MMA-issuing
+// warps (S and dP; then the gradient MMAs).  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,11 +38,7 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 64;
-constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
-#ifndef SPARGE_BWD_POLY_EVERY
-#define SPARGE_BWD_POLY_EVERY 0
-#endif
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 template <int D>
@@ -132,38 +129,46 @@ __global__ void __launch_bounds__(kOrderThreads) order_by_count_kernel(
   }
 }
 
-// Loads 64 fp32 columns of one TMEM lane (4 x 16) starting at `addr`.
-__device__ __forceinline__ void tmem_ld64(uint32_t addr, float (&x)[64]) {
-  uint32_t ra[16], rb[16], rc[16], rd[16];
-  SPARGE_TMEM_LD_X16(addr + 0, ra);
-  SPARGE_TMEM_LD_X16(addr + 16, rb);
-  SPARGE_TMEM_LD_X16(addr + 32, rc);
-  SPARGE_TMEM_LD_X16(addr + 48, rd);
-  SPARGE_TMEM_WAIT_LD16(ra);
-  SPARGE_TMEM_WAIT_LD16(rb);
-  SPARGE_TMEM_WAIT_LD16(rc);
-  SPARGE_TMEM_WAIT_LD16(rd);
+// Writes 32 bf16 values (half of a 128-byte row: 16-byte chunks 4h .. 4h+3)
+// into a 128-byte-swizzled tile.
+__device__ __forceinline__ void store_half_row_sw128(uint8_t* tile, int row, int half,
+                                                     const uint32_t (&pk)[16]) {
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    x[c] = __uint_as_float(ra[c]);
-    x[16 + c] = __uint_as_float(rb[c]);
-    x[32 + c] = __uint_as_float(rc[c]);
-    x[48 + c] = __uint_as_float(rd[c]);
-  }
-}
-
-// Writes 64 bf16 values (one 128-byte row) into a 128-byte-swizzled tile.
-__device__ __forceinline__ void store_row_sw128(uint8_t* tile, int row, const uint32_t (&pk)[32]) {
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
+  for (int ch = 0; ch < 4; ++ch) {
     uint4 v;
     v.x = pk[4 * ch + 0];
     v.y = pk[4 * ch + 1];
     v.z = pk[4 * ch + 2];
     v.w = pk[4 * ch + 3];
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, ch * 16)) = v;
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, (half * 4 + ch) * 16)) = v;
   }
 }
+
+// Loads 32 fp32 columns of one TMEM lane starting at `addr`.
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&x)[32]) {
+  uint32_t ra[16], rb[16];
+  SPARGE_TMEM_LD_X16(addr + 0, ra);
+  SPARGE_TMEM_LD_X16(addr + 16, rb);
+  SPARGE_TMEM_WAIT_LD16(ra);
+  SPARGE_TMEM_WAIT_LD16(rb);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    x[c] = __uint_as_float(ra[c]);
+    x[16 + c] = __uint_as_float(rb[c]);
+  }
+}
+
+// Warp roles of both gradient kernels (352 threads): warps 0-7 compute, with
+// query row (or feature) 32*(w % 4) + lane = TMEM lane and score columns
+// 32*(w / 4) .. +31 (P comes from the saved LSE, so a row needs no exchange
+// between its two warps); warp 8 TMA producer; warp 9 issues the S and dP
+// MMAs; warp 10 issues the gradient MMAs.  Two issuers let the MMAs of
+// neighbouring tiles overlap.
+constexpr int kGradThreads = 352;
+constexpr int kComputeWarps = 8;
+constexpr int kGProducer = 8;
+constexpr int kGIssueA = 9;
+constexpr int kGIssueB = 10;
 
 // ---------------------------------------------------------------- dK, dV
 template <int D>
@@ -177,16 +182,16 @@ struct DkdvCfg {
   static constexpr uint32_t off_v = off_k + kKV;
   static constexpr uint32_t off_q = off_v + kKV;                 // NST stages of Q
   static constexpr uint32_t off_do = off_q + NST * kQ;           // NST stages of dO
-  static constexpr uint32_t off_p = off_do + NST * kQ;    // 2 buffers
-  static constexpr uint32_t off_ds = off_p + 2 * kP;      // 2 buffers
+  static constexpr uint32_t off_p = off_do + NST * kQ;           // 2 buffers
+  static constexpr uint32_t off_ds = off_p + 2 * kP;             // 2 buffers
   static constexpr uint32_t off_bar = off_ds + 2 * kP;
   static constexpr int B_KV = 0;
   static constexpr int B_QF = 1;
   static constexpr int B_QE = B_QF + NST;
   static constexpr int B_SF = B_QE + NST;  // 2
-  static constexpr int B_PSF = B_SF + 2;   // 2, count 128
+  static constexpr int B_PSF = B_SF + 2;   // 2, count 256
   static constexpr int B_PSE = B_PSF + 2;  // 2
-  static constexpr int B_DONE = B_PSE + 2;
+  static constexpr int B_DONE = B_PSE + 2; // count 2
   static constexpr int NBAR = B_DONE + 1;
   static constexpr uint32_t off_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_slot + 16;
@@ -197,7 +202,7 @@ struct DkdvCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kGradThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const float* __restrict__ lse, const float* __restrict__ delta,
@@ -223,11 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kv_valid = min(kBN, N - j * kBN);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i)
-      mbar_init(bar(i), (i == C::B_PSF || i == C::B_PSF + 1) ? 128u : 1u);
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i == C::B_PSF || i == C::B_PSF + 1) cnt = 32 * kComputeWarps;
+      if (i == C::B_DONE) cnt = 2;
+      mbar_init(bar(i), cnt);
+    }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kGIssueA) {
     tmem_alloc(smem_u32(slot), C::tmem_cols);
     tmem_relinquish();
   }
@@ -236,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *slot;
 
-  if (warp == 4) {
+  if (warp == kGProducer) {
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::kKV);
       for (int c = 0; c < C::KCH; ++c) {
@@ -263,76 +272,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = max(0, issued - C::NST); t < issued; ++t)
         mbar_wait(bar(C::B_QF + t % C::NST), (t / C::NST) & 1, kWaitTimeoutNs);
     }
-  } else if (warp == 5) {
+  } else if (warp == kGIssueA) {
+    // S_t = Q_t K^T and dP_t = dO_t V^T (M = 128 query rows, N = 64 keys).
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);   // [q x kv], K = d
-      constexpr uint32_t idG = idesc_bf16(kBM, kBN, true, true);     // [d x kv], K = q
+      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
       bool ok = mbar_wait(bar(C::B_KV), 0, kWaitTimeoutNs);
-      for (int t = 0; ok && t <= n; ++t) {
-        if (t < n) {
-          const int s = t % C::NST;
-          if (!mbar_wait(bar(C::B_QF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t qb = s0 + C::off_q + s * C::kQ;
-          const uint32_t ob = s0 + C::off_do + s * C::kQ;
-          const uint32_t dS = tmem + (t & 1) * 128;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-            const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-            tc_mma_bf16(dS, sdesc_sw128(qb + ko, 16, 1024),
-                        sdesc_sw128(s0 + C::off_k + kko, 16, 1024), idS, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-            const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-            tc_mma_bf16(dS + 64, sdesc_sw128(ob + ko, 16, 1024),
-                        sdesc_sw128(s0 + C::off_v + kko, 16, 1024), idS, kk > 0);
-          }
-          tc_commit(bar(C::B_SF + (t & 1)));
+      for (int t = 0; ok && t < n; ++t) {
+        const int s = t % C::NST;
+        // TMEM buffer t & 1 was read by the compute warps of tile t - 2 before
+        // they filled P/dS(t - 2).
+        if (!mbar_wait(bar(C::B_QF + s), (t / C::NST) & 1, kWaitTimeoutNs) ||
+            (t >= 2 && !mbar_wait(bar(C::B_PSF + (t & 1)), ((t - 2) >> 1) & 1, kWaitTimeoutNs))) {
+          ok = false;
+          break;
         }
-        if (t >= 1) {
-          const int u = t - 1;
-          const int su = u % C::NST;
-          const int pb = u & 1;
-          if (!mbar_wait(bar(C::B_PSF + pb), (u >> 1) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t qb = s0 + C::off_q + su * C::kQ;
-          const uint32_t ob = s0 + C::off_do + su * C::kQ;
-          const uint32_t pbuf = s0 + C::off_p + pb * C::kP;
-          const uint32_t dsbuf = s0 + C::off_ds + pb * C::kP;
+        tc_fence_after();
+        const uint32_t qb = s0 + C::off_q + s * C::kQ;
+        const uint32_t ob = s0 + C::off_do + s * C::kQ;
+        const uint32_t dS = tmem + (t & 1) * 128;
 #pragma unroll
-          for (int kk = 0; kk < kBM / 16; ++kk) {
-            // A = dO^T (M = d, MN-major: 64-element chunks kBM*128 apart),
-            // B = P (N = kv, MN-major); K = 16 query rows per step.
-            tc_mma_bf16(tmem + C::col_dv, sdesc_sw128(ob + kk * 2048, kBM * 128, 1024),
-                        sdesc_sw128(pbuf + kk * 2048, kBM * 128, 1024), idG,
-                        (u > 0 || kk > 0) ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < kBM / 16; ++kk) {
-            tc_mma_bf16(tmem + C::col_dk, sdesc_sw128(qb + kk * 2048, kBM * 128, 1024),
-                        sdesc_sw128(dsbuf + kk * 2048, kBM * 128, 1024), idG,
-                        (u > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(bar(C::B_QE + su));
-          tc_commit(bar(C::B_PSE + pb));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+          tc_mma_bf16(dS, sdesc_sw128(qb + ko, 16, 1024),
+                      sdesc_sw128(s0 + C::off_k + kko, 16, 1024), idS, kk > 0);
         }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+          tc_mma_bf16(dS + 64, sdesc_sw128(ob + ko, 16, 1024),
+                      sdesc_sw128(s0 + C::off_v + kko, 16, 1024), idS, kk > 0);
+        }
+        tc_commit(bar(C::B_SF + (t & 1)));
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+      tc_commit(bar(C::B_DONE));
+      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+    }
+  } else if (warp == kGIssueB) {
+    // dV^T += dO_u^T P_u and dK^T += Q_u^T dS_u (M = d, N = 64 keys, K = 16
+    // query rows per step; A and B read MN-major).
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idG = idesc_bf16(kBM, kBN, true, true);
+      bool ok = true;
+      for (int u = 0; ok && u < n; ++u) {
+        const int su = u % C::NST;
+        const int pb = u & 1;
+        if (!mbar_wait(bar(C::B_PSF + pb), (u >> 1) & 1, kWaitTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t qb = s0 + C::off_q + su * C::kQ;
+        const uint32_t ob = s0 + C::off_do + su * C::kQ;
+        const uint32_t pbuf = s0 + C::off_p + pb * C::kP;
+        const uint32_t dsbuf = s0 + C::off_ds + pb * C::kP;
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          tc_mma_bf16(tmem + C::col_dv, sdesc_sw128(ob + kk * 2048, kBM * 128, 1024),
+                      sdesc_sw128(pbuf + kk * 2048, kBM * 128, 1024), idG,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          tc_mma_bf16(tmem + C::col_dk, sdesc_sw128(qb + kk * 2048, kBM * 128, 1024),
+                      sdesc_sw128(dsbuf + kk * 2048, kBM * 128, 1024), idG,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+        // S/dP(u) completed before P/dS(u) were written, so the Q/dO stage is
+        // free once these MMAs complete.
+        tc_commit(bar(C::B_QE + su));
+        tc_commit(bar(C::B_PSE + pb));
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
   } else {
-    const int r = threadIdx.x;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const int c0 = half * 32;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     bool ok = true;
     // Two-deep prefetch: the q-block index of tile t+2 and the LSE / D of
     // tile t+1 are loaded while tile t is computed.
@@ -361,17 +380,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t pk[32], dk_[32];
+      uint32_t pk[16], dk_[16];
       {
-        float s[64], dp[64];
-        tmem_ld64(lane_base + (t & 1) * 128, s);
-        tmem_ld64(lane_base + (t & 1) * 128 + 64, dp);
+        float s[32], dp[32];
+        tmem_ld32(lane_base + (t & 1) * 128 + c0, s);
+        tmem_ld32(lane_base + (t & 1) * 128 + 64 + c0, dp);
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float p0 = exp2_split<SPARGE_BWD_POLY_EVERY>(c, fmaf(s[c], scale_log2, -lse2));
-          float p1 = exp2_split<SPARGE_BWD_POLY_EVERY>(c + 1, fmaf(s[c + 1], scale_log2, -lse2));
-          if (!rv || c >= kv_valid) p0 = 0.f;
-          if (!rv || c + 1 >= kv_valid) p1 = 0.f;
+        for (int c = 0; c < 32; c += 2) {
+          float p0 = ex2_approx(fmaf(s[c], scale_log2, -lse2));
+          float p1 = ex2_approx(fmaf(s[c + 1], scale_log2, -lse2));
+          if (!rv || c0 + c >= kv_valid) p0 = 0.f;
+          if (!rv || c0 + c + 1 >= kv_valid) p1 = 0.f;
           pk[c / 2] = pack_bf16x2(p0, p1);
           dk_[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
         }
@@ -381,14 +400,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      store_row_sw128(sm + C::off_p + (t & 1) * C::kP, r, pk);
-      store_row_sw128(sm + C::off_ds + (t & 1) * C::kP, r, dk_);
+      store_half_row_sw128(sm + C::off_p + (t & 1) * C::kP, r, half, pk);
+      store_half_row_sw128(sm + C::off_ds + (t & 1) * C::kP, r, half, dk_);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_PSF + (t & 1)));
     }
     if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-    // Epilogue: thread r holds column r of dV^T / dK^T (= feature r of 64 kv rows).
+    // Epilogue: lane r holds feature r of dV^T / dK^T; this warp writes the 32
+    // keys c0 .. c0+31 of it.
     bool have = ok && n > 0;
     if (have) {
       have = warp_wait(bar(C::B_PSE + ((n - 1) & 1)), ((n - 1) >> 1) & 1);
@@ -397,11 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const long long base = ((long long)bh * N + (long long)j * kBN) * D + r;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kBN; c0 += 16) {
+    for (int cc = c0; cc < c0 + 32; cc += 16) {
       uint32_t rv_[16], rk_[16];
       if (have) {
-        SPARGE_TMEM_LD_X16(lane_base + C::col_dv + c0, rv_);
-        SPARGE_TMEM_LD_X16(lane_base + C::col_dk + c0, rk_);
+        SPARGE_TMEM_LD_X16(lane_base + C::col_dv + cc, rv_);
+        SPARGE_TMEM_LD_X16(lane_base + C::col_dk + cc, rk_);
         SPARGE_TMEM_WAIT_LD16(rv_);
         SPARGE_TMEM_WAIT_LD16(rk_);
       } else {
@@ -411,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r < D) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          if (c0 + c < kv_valid) {
-            dv[base + (long long)(c0 + c) * D] = __float2bfloat16_rn(__uint_as_float(rv_[c]));
-            dk[base + (long long)(c0 + c) * D] =
+          if (cc + c < kv_valid) {
+            dv[base + (long long)(cc + c) * D] = __float2bfloat16_rn(__uint_as_float(rv_[c]));
+            dk[base + (long long)(cc + c) * D] =
                 __float2bfloat16_rn(__uint_as_float(rk_[c]) * scale);
           }
         }
@@ -423,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kGIssueA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::tmem_cols);
   }
@@ -432,35 +452,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------- dQ
 template <int D>
 struct DqCfg {
-  static constexpr int NST = 3;
   static constexpr int KCH = D / 64;
   static constexpr uint32_t kKV = kBN * D * 2;
   static constexpr uint32_t kQ = kBM * D * 2;
   static constexpr uint32_t kP = kBM * kBN * 2;
+  // With d = 128, dS_t goes into the V tile of its own stage (V_t is dead once
+  // dP_t has completed; the stage is not reloaded before dQ_t completes).
+  static constexpr bool DS_IN_V = kKV >= kP;
+  static constexpr int NST = DS_IN_V ? 4 : 3;
   static constexpr uint32_t off_q = 0;
   static constexpr uint32_t off_do = off_q + kQ;
   static constexpr uint32_t off_k = off_do + kQ;
   static constexpr uint32_t off_v = off_k + NST * kKV;
-  static constexpr uint32_t off_ds = off_v + NST * kKV;  // 2 buffers
-  static constexpr uint32_t off_bar = off_ds + 2 * kP;
+  static constexpr uint32_t off_ds = off_v + NST * kKV;  // 2 buffers unless DS_IN_V
+  static constexpr uint32_t off_bar = off_ds + (DS_IN_V ? 0 : 2 * kP);
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;
   static constexpr int B_VF = B_KF + NST;
   static constexpr int B_KE = B_VF + NST;
   static constexpr int B_SF = B_KE + NST;   // 2
-  static constexpr int B_DSF = B_SF + 2;    // 2, count 128
+  static constexpr int B_DSF = B_SF + 2;    // 2, count 256
   static constexpr int B_DSE = B_DSF + 2;   // 2
-  static constexpr int B_DONE = B_DSE + 2;
+  static constexpr int B_DONE = B_DSE + 2;  // count 2
   static constexpr int NBAR = B_DONE + 1;
   static constexpr uint32_t off_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_slot + 16;
   static constexpr uint32_t smem_alloc = bytes + 1024;
   static constexpr uint32_t tmem_cols = 512;  // S/dP x2 [0,256), dQ [256, 256+D)
   static constexpr uint32_t col_dq = 256;
+  __device__ static uint32_t ds_addr(uint32_t s0, int t) {
+    return DS_IN_V ? s0 + off_v + (t % NST) * kKV : s0 + off_ds + (t & 1) * kP;
+  }
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kGradThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const float* __restrict__ lse, const float* __restrict__ delta,
@@ -484,11 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* list = row_idx + row_id * Mk;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i)
-      mbar_init(bar(i), (i == C::B_DSF || i == C::B_DSF + 1) ? 128u : 1u);
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i == C::B_DSF || i == C::B_DSF + 1) cnt = 32 * kComputeWarps;
+      if (i == C::B_DONE) cnt = 2;
+      mbar_init(bar(i), cnt);
+    }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kGIssueA) {
     tmem_alloc(smem_u32(slot), C::tmem_cols);
     tmem_relinquish();
   }
@@ -497,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *slot;
 
-  if (warp == 4) {
+  if (warp == kGProducer) {
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::kQ);
       for (int c = 0; c < C::KCH; ++c) {
@@ -527,69 +557,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(C::B_VF + t % C::NST), (t / C::NST) & 1, kWaitTimeoutNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kGIssueA) {
+    // S_t = Q K_t^T and dP_t = dO V_t^T.
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t idQ = idesc_bf16(kBM, D, false, true);
       bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
-      for (int t = 0; ok && t <= n; ++t) {
-        if (t < n) {
-          const int s = t % C::NST;
-          const uint32_t dS = tmem + (t & 1) * 128;
-          if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-            const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-            tc_mma_bf16(dS, sdesc_sw128(s0 + C::off_q + ko, 16, 1024),
-                        sdesc_sw128(s0 + C::off_k + s * C::kKV + kko, 16, 1024), idS, kk > 0);
-          }
-          if (!mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-            const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-            tc_mma_bf16(dS + 64, sdesc_sw128(s0 + C::off_do + ko, 16, 1024),
-                        sdesc_sw128(s0 + C::off_v + s * C::kKV + kko, 16, 1024), idS, kk > 0);
-          }
-          tc_commit(bar(C::B_SF + (t & 1)));
+      for (int t = 0; ok && t < n; ++t) {
+        const int s = t % C::NST;
+        const uint32_t dS = tmem + (t & 1) * 128;
+        // TMEM buffer t & 1 was read by the compute warps of tile t - 2 before
+        // they filled dS(t - 2).
+        if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs) ||
+            (t >= 2 && !mbar_wait(bar(C::B_DSF + (t & 1)), ((t - 2) >> 1) & 1, kWaitTimeoutNs))) {
+          ok = false;
+          break;
         }
-        if (t >= 1) {
-          const int u = t - 1;
-          const int su = u % C::NST;
-          if (!mbar_wait(bar(C::B_DSF + (u & 1)), (u >> 1) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t dsb = s0 + C::off_ds + (u & 1) * C::kP;
-          const uint32_t kb = s0 + C::off_k + su * C::kKV;
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            // A = dS (K-major, K = kv), B = K_j (N = d, MN-major).
-            tc_mma_bf16(tmem + C::col_dq, sdesc_sw128(dsb + kk * 32, 16, 1024),
-                        sdesc_sw128(kb + kk * 2048, kBN * 128, 1024), idQ,
-                        (u > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(bar(C::B_KE + su));
-          tc_commit(bar(C::B_DSE + (u & 1)));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+          tc_mma_bf16(dS, sdesc_sw128(s0 + C::off_q + ko, 16, 1024),
+                      sdesc_sw128(s0 + C::off_k + s * C::kKV + kko, 16, 1024), idS, kk > 0);
         }
+        if (!mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+          tc_mma_bf16(dS + 64, sdesc_sw128(s0 + C::off_do + ko, 16, 1024),
+                      sdesc_sw128(s0 + C::off_v + s * C::kKV + kko, 16, 1024), idS, kk > 0);
+        }
+        tc_commit(bar(C::B_SF + (t & 1)));
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+      tc_commit(bar(C::B_DONE));
+      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+    }
+  } else if (warp == kGIssueB) {
+    // dQ += dS_u K_u (A = dS K-major with K = 64 keys, B = K_u MN-major, N = d).
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idQ = idesc_bf16(kBM, D, false, true);
+      bool ok = true;
+      for (int u = 0; ok && u < n; ++u) {
+        const int su = u % C::NST;
+        if (!mbar_wait(bar(C::B_DSF + (u & 1)), (u >> 1) & 1, kWaitTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dsb = C::ds_addr(s0, u);
+        const uint32_t kb = s0 + C::off_k + su * C::kKV;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          tc_mma_bf16(tmem + C::col_dq, sdesc_sw128(dsb + kk * 32, 16, 1024),
+                      sdesc_sw128(kb + kk * 2048, kBN * 128, 1024), idQ,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+        // S/dP(u) completed before dS(u) was written, so stage su is free
+        // once this MMA completes.
+        tc_commit(bar(C::B_KE + su));
+        tc_commit(bar(C::B_DSE + (u & 1)));
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
   } else {
-    const int r = threadIdx.x;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const int c0 = half * 32;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int row = qb * kBM + r;
     const bool rv = row < N;
     const float lse2 = (rv && n > 0) ? __ldg(lse + (long long)bh * N + row) * kLog2e : 0.f;
@@ -605,25 +646,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t pk[32];
+      uint32_t pk[16];
       {
-        float s[64], dp[64];
-        tmem_ld64(lane_base + (t & 1) * 128, s);
-        tmem_ld64(lane_base + (t & 1) * 128 + 64, dp);
+        float s[32], dp[32];
+        tmem_ld32(lane_base + (t & 1) * 128 + c0, s);
+        tmem_ld32(lane_base + (t & 1) * 128 + 64 + c0, dp);
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float p0 = exp2_split<SPARGE_BWD_POLY_EVERY>(c, fmaf(s[c], scale_log2, -lse2));
-          float p1 = exp2_split<SPARGE_BWD_POLY_EVERY>(c + 1, fmaf(s[c + 1], scale_log2, -lse2));
-          if (!rv || c >= kv_valid) p0 = 0.f;
-          if (!rv || c + 1 >= kv_valid) p1 = 0.f;
+        for (int c = 0; c < 32; c += 2) {
+          float p0 = ex2_approx(fmaf(s[c], scale_log2, -lse2));
+          float p1 = ex2_approx(fmaf(s[c + 1], scale_log2, -lse2));
+          if (!rv || c0 + c >= kv_valid) p0 = 0.f;
+          if (!rv || c0 + c + 1 >= kv_valid) p1 = 0.f;
           pk[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
         }
       }
-      if (t >= 2 && !warp_wait(bar(C::B_DSE + (t & 1)), ((t - 2) >> 1) & 1)) {
+      if (!C::DS_IN_V && t >= 2 && !warp_wait(bar(C::B_DSE + (t & 1)), ((t - 2) >> 1) & 1)) {
         ok = false;
         break;
       }
-      store_row_sw128(sm + C::off_ds + (t & 1) * C::kP, r, pk);
+      store_half_row_sw128(sm + (C::ds_addr(s0, t) - s0), r, half, pk);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSF + (t & 1)));
@@ -637,10 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     __nv_bfloat16* qrow = dq + ((long long)bh * N + row) * D;
 #pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 16) {
+    for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 16) {
       uint32_t ro[16];
       if (have) {
-        SPARGE_TMEM_LD_X16(lane_base + C::col_dq + c0, ro);
+        SPARGE_TMEM_LD_X16(lane_base + C::col_dq + cc, ro);
         SPARGE_TMEM_WAIT_LD16(ro);
       } else {
 #pragma unroll
@@ -656,15 +697,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       w1.z = pack_bf16x2(__uint_as_float(ro[12]) * scale, __uint_as_float(ro[13]) * scale);
       w1.w = pack_bf16x2(__uint_as_float(ro[14]) * scale, __uint_as_float(ro[15]) * scale);
       if (rv) {
-        *reinterpret_cast<uint4*>(qrow + c0) = w0;
-        *reinterpret_cast<uint4*>(qrow + c0 + 8) = w1;
+        *reinterpret_cast<uint4*>(qrow + cc) = w0;
+        *reinterpret_cast<uint4*>(qrow + cc + 8) = w1;
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kGIssueA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::tmem_cols);
   }
@@ -703,7 +744,7 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DkdvCfg<D>::smem_alloc);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mk), kThreads,
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mk), kGradThreads,
                        DkdvCfg<D>::smem_alloc, st>>>(
       tq, tk, tv, tdo, lse, delta, col_idx, col_cnt, ws.col_order, g.N, g.Mq, g.Mk, scale,
       scale_log2,
@@ -714,7 +755,7 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DqCfg<D>::smem_alloc);
   if (e != cudaSuccess) return e;
-  bwd_dq_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mq), kThreads, DqCfg<D>::smem_alloc,
+  bwd_dq_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mq), kGradThreads, DqCfg<D>::smem_alloc,
                      st>>>(tq, tk, tv, tdo, lse, delta, row_idx, row_cnt, ws.row_order, g.N, g.Mq,
                            g.Mk, scale, scale_log2, static_cast<__nv_bfloat16*>(dq), status);
   return cudaGetLastError();

@@ -230,15 +230,6 @@ SPARGE_DEV float exp2_poly(float x) {
   return x < -126.f ? 0.f : r;
 }
 
-// Columns c of a 64-wide score row whose exp2 runs on the FMA pipe: every
-// kPolyEvery-th column (0 = none).  Tuned per kernel by measurement.
-template <int kPolyEvery>
-SPARGE_DEV float exp2_split(int c, float x) {
-  if (kPolyEvery > 0 && (c % (kPolyEvery > 0 ? kPolyEvery : 1)) == (kPolyEvery > 0 ? kPolyEvery - 1 : 0))
-    return exp2_poly(x);
-  return ex2_approx(x);
-}
-
 SPARGE_DEV uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
 }  // namespace sparge
