@@ -39,7 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = ("sparse attn fwd+bwd ms & kept-FLOP TFLOP/s at 95% sparsity; "
           "% of BF16/HBM roofline")
-KERNELS_PER_STEP = 7  # pool, score+select, csc, fwd, delta, dkdv, dq
+KERNELS_PER_STEP = 9  # pool, select, csc, fwd, delta, 2 x order-by-count, dkdv, dq
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

@@ -87,6 +87,8 @@ int check_kp(float k_frac, float p) {
   return SPARGE_OK;
 }
 
+// Mask workspace: Q means [BH, Mq, d] and K means transposed [BH, d, Mk],
+// both fp32.
 size_t mask_ws_bytes(const Geom& g) {
   return round_up((size_t)g.BH * g.Mq * g.d * sizeof(float)) +
          round_up((size_t)g.BH * g.d * g.Mk * sizeof(float));
@@ -149,7 +151,7 @@ int sparge_pool(const sparge_shape* shape, const void* q, const void* k, float* 
   SPARGE_TRY(check_opt_word(qbar));
   SPARGE_TRY(check_opt_word(kbar));
   const Geom g = make_geom(*shape);
-  return cuda_status(launch_pool(g, q, k, qbar, kbar, nullptr, stream));
+  return cuda_status(launch_pool(g, q, k, qbar, kbar, stream));
 }
 
 int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes) {
@@ -163,11 +165,11 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
                 float softmax_scale, uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
                 int32_t* col_idx, int32_t* col_cnt, float* pooled_logit, float* pooled_prob,
                 void* workspace, size_t ws_bytes, int32_t* status, sparge_stream_t stream) {
-  (void)status;  // the mask kernels have no internal waits
   SPARGE_TRY(check_shape(shape));
   SPARGE_TRY(check_tensor(q));
   SPARGE_TRY(check_tensor(k));
   SPARGE_TRY(check_kp(k_frac, p));
+  SPARGE_TRY(check_opt_word(status));  // accepted for symmetry; the mask has no waits
   if (!isfinite(softmax_scale)) return SPARGE_ERR_INVALID_ARG;
   SPARGE_TRY(check_word(bitmask));
   SPARGE_TRY(check_word(row_idx));
@@ -183,14 +185,11 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
 
   float* qbar = static_cast<float*>(workspace);
   float* kbarT = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                          round_up((size_t)g.BH * g.Mq * g.d * sizeof(float)));
+                                           round_up((size_t)g.BH * g.Mq * g.d * sizeof(float)));
   const float scale = resolve_scale(softmax_scale, g.d);
-  SPARGE_TRY(cuda_status(launch_pool(g, q, k, qbar, nullptr, kbarT, stream)));
-  SPARGE_TRY(cuda_status(launch_score_select(g, qbar, kbarT, scale, topk_blocks(k_frac, g.Mk), p,
-                                             bitmask, row_idx, row_cnt, pooled_logit,
-                                             pooled_prob, stream)));
-  if (col_idx) SPARGE_TRY(cuda_status(launch_csc(g, bitmask, col_idx, col_cnt, stream)));
-  return SPARGE_OK;
+  return cuda_status(launch_mask_pipeline(g, q, k, qbar, kbarT, scale, topk_blocks(k_frac, g.Mk),
+                                          p, bitmask, row_idx, row_cnt, col_idx, col_cnt,
+                                          pooled_logit, pooled_prob, stream));
 }
 
 int sparge_mask_from_prob(const sparge_shape* shape, const float* prob, float k_frac, float p,

@@ -22,16 +22,19 @@ int select_rows_per_cta(int Mk);
 
 // pool.cu / mask.cu
 cudaError_t launch_pool(const Geom& g, const void* q, const void* k, float* qbar, float* kbar,
-                        float* kbarT, cudaStream_t st);
-cudaError_t launch_score_select(const Geom& g, const float* qbar, const float* kbarT, float scale,
-                                int ktop, float p, uint32_t* bitmask, int32_t* row_idx,
-                                int32_t* row_cnt, float* logit_out, float* prob_out,
-                                cudaStream_t st);
+                        cudaStream_t st);
 cudaError_t launch_select_from_prob(const Geom& g, const float* prob, int ktop, float p,
                                     uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
                                     cudaStream_t st);
 cudaError_t launch_csc(const Geom& g, const uint32_t* bitmask, int32_t* col_idx, int32_t* col_cnt,
                        cudaStream_t st);
+// The mask as three kernels chained by programmatic dependent launch
+// (mask.cu); kbarT receives the K means transposed, [BH, d, Mk].
+cudaError_t launch_mask_pipeline(const Geom& g, const void* q, const void* k, float* qbar,
+                                 float* kbarT, float scale, int ktop, float p, uint32_t* bitmask,
+                                 int32_t* row_idx, int32_t* row_cnt, int32_t* col_idx,
+                                 int32_t* col_cnt, float* logit_out, float* prob_out,
+                                 cudaStream_t st);
 
 // attn_fwd.cu
 cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const void* v,

@@ -8,9 +8,9 @@
 // Kernel-Implementierung und Modellanpassung" (mask construction in CUDA).
 //
 // Kernels:
-//   pool_kernel          HBM-bound block means of Q and K (16-byte loads).
-//   score_select_kernel  pooled logits (fp32 FMA), row softmax, hybrid
-//                        selection; emits the bitmask and the CSR lists.
+//   pool_kernel, select_kernel, csc_split_kernel  the sparge_mask pipeline
+//                        (see "mask pipeline" below); pool_kernel alone also
+//                        serves sparge_pool.
 //   select_from_prob_kernel  the selection alone on a given probability map.
 //   csc_kernel           transposes the bitmask into per-kv-block q lists.
 //
@@ -28,6 +28,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -42,29 +44,16 @@ constexpr int kSelLogitFloats = 20480;         // 80 KB of logits per CTA
 constexpr unsigned kFull = 0xffffffffu;
 
 // ---------------------------------------------------------------- pooling
-// One CTA per (head, block) unit.  Units [0, BH*Mq) are Q blocks, the rest K
-// blocks.  Thread t reads 16-byte chunk (t % CH) of rows t / CH, + RG, ...
+// Mean of `rows` rows of one block (d = D bf16 values per row), written to
+// out[t * stride] for channel t.  Thread i reads 16-byte chunk (i % CH) of
+// rows i / CH, + RG, ...; the partial sums meet in `red`.  The caller
+// synchronises before reusing `red`.
 template <int D>
-__global__ void __launch_bounds__(kPoolThreads) pool_kernel(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int BH, int N,
-    int bq, int bk, int Mq, int Mk, int do_q, int do_k, float* __restrict__ qbar,
-    float* __restrict__ kbar, float* __restrict__ kbarT) {
+__device__ __forceinline__ void pool_block(const __nv_bfloat16* __restrict__ src, int rows,
+                                           float (*red)[D], float* __restrict__ out,
+                                           long long stride) {
   constexpr int CH = D / 8;              // 16-byte chunks per row
   constexpr int RG = kPoolThreads / CH;  // rows read concurrently
-  __shared__ float red[RG][D];
-
-  const long long unit = blockIdx.x;
-  const long long nq = do_q ? (long long)BH * Mq : 0;
-  const bool is_q = unit < nq;
-  const long long u = is_q ? unit : unit - nq;
-  const int M = is_q ? Mq : Mk;
-  const int blk = is_q ? bq : bk;
-  const int bh = static_cast<int>(u / M);
-  const int i = static_cast<int>(u % M);
-  const int r0 = i * blk;
-  const int rows = min(blk, N - r0);
-  const __nv_bfloat16* src = (is_q ? q : k) + ((long long)bh * N + r0) * D;
-
   const int c = threadIdx.x % CH;
   const int rg = threadIdx.x / CH;
   float acc[8];
@@ -90,14 +79,39 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(
     float s = 0.f;
 #pragma unroll
     for (int g = 0; g < RG; ++g) s += red[g][threadIdx.x];
-    const float mean = s / static_cast<float>(rows);
-    if (is_q) {
-      qbar[((long long)bh * Mq + i) * D + threadIdx.x] = mean;
-    } else {
-      if (kbar) kbar[((long long)bh * Mk + i) * D + threadIdx.x] = mean;
-      if (kbarT) kbarT[((long long)bh * D + threadIdx.x) * Mk + i] = mean;
-    }
+    out[threadIdx.x * stride] = s / static_cast<float>(rows);
   }
+}
+
+// One CTA per (head, block) unit.  Units [0, BH*Mq) are Q blocks, the rest K
+// blocks.  Q means are row-major [BH, Mq, d]; K means row-major [BH, Mk, d]
+// into kbar, or transposed [BH, d, Mk] into kbarT when that is set.
+template <int D>
+__global__ void __launch_bounds__(kPoolThreads) pool_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int BH, int N,
+    int bq, int bk, int Mq, int Mk, int do_q, float* __restrict__ qbar,
+    float* __restrict__ kbar, float* __restrict__ kbarT) {
+  // Lets a kernel launched with programmatic serialization start early; it
+  // waits for this grid's results itself.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float red[kPoolThreads / (D / 8)][D];
+  const long long unit = blockIdx.x;
+  const long long nq = do_q ? (long long)BH * Mq : 0;
+  const bool is_q = unit < nq;
+  const long long u = is_q ? unit : unit - nq;
+  const int M = is_q ? Mq : Mk;
+  const int blk = is_q ? bq : bk;
+  const int bh = static_cast<int>(u / M);
+  const int i = static_cast<int>(u % M);
+  const int r0 = i * blk;
+  const __nv_bfloat16* src = (is_q ? q : k) + ((long long)bh * N + r0) * D;
+  const int rows = min(blk, N - r0);
+  if (is_q)
+    pool_block<D>(src, rows, red, qbar + ((long long)bh * Mq + i) * D, 1);
+  else if (kbarT)
+    pool_block<D>(src, rows, red, kbarT + (long long)bh * D * Mk + i, Mk);
+  else
+    pool_block<D>(src, rows, red, kbar + ((long long)bh * Mk + i) * D, 1);
 }
 
 // ---------------------------------------------------------------- selection
@@ -261,90 +275,166 @@ __device__ void select_row(const float* prow, int Mk, int ktop, float p, uint32_
   if (lane == 0) *cnt_out = kept;
 }
 
+// Exact warp sum of per-lane partial sums below 2^46 (u <= 2^40, at most 64
+// terms per lane): the three pieces v >> 42, bits 21..41 and bits 0..20 each
+// sum over 32 lanes to less than 2^26, exact in 32-bit reductions.
+__device__ __forceinline__ unsigned long long warp_sum_u42(unsigned long long v) {
+  const uint32_t a = __reduce_add_sync(kFull, static_cast<uint32_t>(v >> 42));
+  const uint32_t b = __reduce_add_sync(kFull, static_cast<uint32_t>((v >> 21) & 0x1fffffu));
+  const uint32_t c = __reduce_add_sync(kFull, static_cast<uint32_t>(v & 0x1fffffu));
+  return (static_cast<unsigned long long>(a) << 42) + (static_cast<unsigned long long>(b) << 21) + c;
+}
+
+// Hybrid Top-k + Top-p selection of one row (one warp), keys in registers.
+// Lane l holds elements j = 32 e + l (e < EPL).  The thresholds are found by
+// a bitwise binary search on the fp32 key: the largest key tau with
+// sum_{key >= tau} u >= Ti (Top-p) or #{key >= tau} >= c (Top-k/union);
+// absent elements carry key 0, which no candidate (>= 1) admits.  Results
+// equal select_row's exactly (same integer rule, same tie order).
+template <int EPL, bool kRegs>
+__device__ void select_row_reg(const float* prow, int Mk, int ktop, float p,
+                               uint32_t* __restrict__ bm_row, int32_t* __restrict__ idx_row,
+                               int32_t* __restrict__ cnt_out) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t* keys = reinterpret_cast<const uint32_t*>(prow);
+  // Elements per lane actually present (EPL is the compile-time bound).  The
+  // loops below unroll fully over EPL so that kr[] stays in registers; in
+  // shared-memory mode they stop at ne.
+  const int ne = kRegs ? EPL : (Mk + 31) / 32;
+  uint32_t kr[kRegs ? EPL : 1];
+  if (kRegs) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const int j = e * 32 + lane;
+      kr[kRegs ? e : 0] = j < Mk ? keys[j] : 0u;
+    }
+  }
+  // Element e of this lane (absent elements read as key 0).
+  auto key_of = [&](int e) -> uint32_t {
+    if (kRegs) return kr[kRegs ? e : 0];
+    const int j = e * 32 + lane;
+    return j < Mk ? keys[j] : 0u;
+  };
+  auto u_of = [&](int, uint32_t k) -> unsigned long long { return fixed40(k); };
+  int m_p;
+  if (p >= 1.f) {
+    m_p = Mk;
+  } else if (!(p > 0.f)) {
+    m_p = 0;
+  } else {
+    unsigned long long part = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      if (!kRegs && e >= ne) break;
+      part += u_of(e, key_of(e));
+    }
+    const unsigned long long U = warp_sum_u42(part);
+    const double T = __dmul_rn(static_cast<double>(p), static_cast<double>(U));
+    const unsigned long long Ti = static_cast<unsigned long long>(ceil(T));
+    if (Ti == 0ull) {
+      m_p = 0;
+    } else {
+      uint32_t tau = 0;
+      for (int bit = 30; bit >= 0; --bit) {
+        const uint32_t cand = tau | (1u << bit);
+        unsigned long long s = 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          if (!kRegs && e >= ne) break;
+          const uint32_t k = key_of(e);
+          s += k >= cand ? u_of(e, k) : 0ull;
+        }
+        if (warp_sum_u42(s) >= Ti) tau = cand;
+      }
+      unsigned long long a = 0;
+      uint32_t cgt = 0;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        if (!kRegs && e >= ne) break;
+        const uint32_t k = key_of(e);
+        const bool gt = k > tau;
+        a += gt ? u_of(e, k) : 0ull;
+        cgt += gt ? 1u : 0u;
+      }
+      const unsigned long long A = warp_sum_u42(a);
+      const uint32_t C = __reduce_add_sync(kFull, cgt);
+      const unsigned long long ut = fixed40(tau);
+      const unsigned long long need = (ut > 0ull && Ti > A) ? (Ti - A + ut - 1ull) / ut : 1ull;
+      m_p = static_cast<int>(min(static_cast<unsigned long long>(Mk), C + need));
+    }
+  }
+  const int c = min(Mk, max(ktop, m_p));
+  // tau_c: a key with exactly c keys >= it if one exists (the search stops
+  // there), else the c-th largest key; either way the kept set below is the
+  // c keys >= tau_c, ties at tau_c taken by lower index.
+  uint32_t tau_c = 0;
+  for (int bit = 30; bit >= 0; --bit) {
+    const uint32_t cand = tau_c | (1u << bit);
+    uint32_t n = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      if (!kRegs && e >= ne) break;
+      n += key_of(e) >= cand ? 1u : 0u;
+    }
+    const int tot = static_cast<int>(__reduce_add_sync(kFull, n));
+    if (tot >= c) {
+      tau_c = cand;
+      if (tot == c) break;
+    }
+  }
+  uint32_t ngt = 0;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    if (!kRegs && e >= ne) break;
+    ngt += key_of(e) > tau_c ? 1u : 0u;
+  }
+  // Keys equal to tau_c are real elements or, when tau_c is 0, zero
+  // probabilities; absent elements are excluded below by j < Mk.
+  const int need_ties = c - static_cast<int>(__reduce_add_sync(kFull, ngt));
+  const uint32_t lt = (1u << lane) - 1u;
+  int ties = 0, kept = 0;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    if (!kRegs && e >= ne) break;
+    const int j = e * 32 + lane;
+    const bool valid = j < Mk;
+    const uint32_t k = key_of(e);
+    const bool gt = valid && k > tau_c;
+    const bool eq = valid && k == tau_c;
+    const uint32_t em = __ballot_sync(kFull, eq);
+    const int rank = ties + __popc(em & lt);
+    const bool keep = gt || (eq && rank < need_ties);
+    ties += __popc(em);
+    const uint32_t km = __ballot_sync(kFull, keep);
+    if (e * 32 < Mk) {
+      if (lane == 0) bm_row[e] = km;
+      if (keep) idx_row[kept + __popc(km & lt)] = j;
+    }
+    kept += __popc(km);
+  }
+  if (lane == 0) *cnt_out = kept;
+}
+
+// Binary search with keys in registers for rows up to 512 blocks, reading
+// them from shared memory up to 2048 blocks, else the radix select.
+__device__ __forceinline__ void select_row_any(const float* prow, int Mk, int ktop, float p,
+                                               uint32_t* hcnt, unsigned long long* hsum,
+                                               uint32_t* bm_row, int32_t* idx_row,
+                                               int32_t* cnt_out) {
+  if (Mk <= 32 * 16)
+    select_row_reg<16, true>(prow, Mk, ktop, p, bm_row, idx_row, cnt_out);
+  else if (Mk <= 32 * 64)
+    select_row_reg<64, false>(prow, Mk, ktop, p, bm_row, idx_row, cnt_out);
+  else
+    select_row(prow, Mk, ktop, p, hcnt, hsum, bm_row, idx_row, cnt_out);
+}
+
 struct SelSmem {
   uint32_t hcnt[kSelMaxRows][256];
   unsigned long long hsum[kSelMaxRows][256];
 };
 
-// Pooled logits + softmax + selection.  CTA = R consecutive q-block rows of
-// one head; grid.x = BH * ceil(Mq / R).
-template <int D>
-__global__ void __launch_bounds__(kSelThreads) score_select_kernel(
-    const float* __restrict__ qbar, const float* __restrict__ kbarT, int Mq, int Mk, int Mkw,
-    int R, float scale, int ktop, float p, uint32_t* __restrict__ bitmask,
-    int32_t* __restrict__ row_idx, int32_t* __restrict__ row_cnt, float* __restrict__ logit_out,
-    float* __restrict__ prob_out) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  SelSmem* hs = reinterpret_cast<SelSmem*>(smem);
-  float* qs = reinterpret_cast<float*>(smem + sizeof(SelSmem));  // [R][D]
-  float* ls = qs + kSelMaxRows * D;                                // [R][Mk]
-
-  const int nrb = (Mq + R - 1) / R;
-  const int bh = blockIdx.x / nrb;
-  const int i0 = (blockIdx.x % nrb) * R;
-  const int nrows = min(R, Mq - i0);
-  const float* qsrc = qbar + ((long long)bh * Mq + i0) * D;
-  for (int t = threadIdx.x; t < kSelMaxRows * D; t += kSelThreads)
-    qs[t] = (t < nrows * D) ? qsrc[t] : 0.f;
-  __syncthreads();
-
-  // Logits: thread owns columns j, accumulates all R rows over d.
-  const float* kt = kbarT + (long long)bh * D * Mk;
-  for (int j = threadIdx.x; j < Mk; j += kSelThreads) {
-    float acc[kSelMaxRows];
-#pragma unroll
-    for (int r = 0; r < kSelMaxRows; ++r) acc[r] = 0.f;
-#pragma unroll 2
-    for (int c = 0; c < D; c += 4) {
-      const float k0 = __ldg(kt + (long long)(c + 0) * Mk + j);
-      const float k1 = __ldg(kt + (long long)(c + 1) * Mk + j);
-      const float k2 = __ldg(kt + (long long)(c + 2) * Mk + j);
-      const float k3 = __ldg(kt + (long long)(c + 3) * Mk + j);
-#pragma unroll
-      for (int r = 0; r < kSelMaxRows; ++r) {
-        const float4 qv = *reinterpret_cast<const float4*>(qs + r * D + c);
-        acc[r] = fmaf(qv.x, k0, acc[r]);
-        acc[r] = fmaf(qv.y, k1, acc[r]);
-        acc[r] = fmaf(qv.z, k2, acc[r]);
-        acc[r] = fmaf(qv.w, k3, acc[r]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kSelMaxRows; ++r)
-      if (r < nrows) ls[r * Mk + j] = acc[r] * scale;
-  }
-  __syncthreads();
-
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (w < nrows) {
-    float* row = ls + w * Mk;
-    const long long grow = (long long)bh * Mq + i0 + w;
-    float m = -INFINITY;
-    for (int j = lane; j < Mk; j += 32) m = fmaxf(m, row[j]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    float s = 0.f;
-    for (int j = lane; j < Mk; j += 32) {
-      const float lg = row[j];
-      if (logit_out) logit_out[grow * Mk + j] = lg;
-      const float e = expf(lg - m);
-      row[j] = e;
-      s += e;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-    for (int j = lane; j < Mk; j += 32) {
-      const float pj = __fdiv_rn(row[j], s);
-      row[j] = pj;
-      if (prob_out) prob_out[grow * Mk + j] = pj;
-    }
-    __syncwarp();
-    select_row(row, Mk, ktop, p, hs->hcnt[w], hs->hsum[w], bitmask + grow * Mkw,
-               row_idx + grow * Mk, row_cnt + grow);
-  }
-}
-
-__global__ void __launch_bounds__(kSelThreads) select_from_prob_kernel(
+__global__ void __launch_bounds__(kSelThreads, 1) select_from_prob_kernel(
     const float* __restrict__ prob, int Mq, int Mk, int Mkw, int R, int ktop, float p,
     uint32_t* __restrict__ bitmask, int32_t* __restrict__ row_idx, int32_t* __restrict__ row_cnt) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -360,7 +450,7 @@ __global__ void __launch_bounds__(kSelThreads) select_from_prob_kernel(
     float* row = ls + w * Mk;
     for (int j = lane; j < Mk; j += 32) row[j] = __ldg(prob + grow * Mk + j);
     __syncwarp();
-    select_row(row, Mk, ktop, p, hs->hcnt[w], hs->hsum[w], bitmask + grow * Mkw,
+    select_row_any(row, Mk, ktop, p, hs->hcnt[w], hs->hsum[w], bitmask + grow * Mkw,
                row_idx + grow * Mk, row_cnt + grow);
   }
 }
@@ -391,9 +481,166 @@ __global__ void __launch_bounds__(kCscThreads) csc_kernel(const uint32_t* __rest
   }
 }
 
-size_t select_smem_bytes(int d, int R, int Mk) {
-  return sizeof(SelSmem) + (size_t)kSelMaxRows * d * sizeof(float) +
-         (size_t)R * Mk * sizeof(float);
+// ---------------------------------------------------------------- mask pipeline
+// sparge_mask runs three kernels chained by programmatic dependent launch:
+//   pool_kernel        Q- and K-block means (HBM-bound, 16-byte loads); for the
+//                      pipeline the K means are stored transposed [BH, d, Mk].
+//   select_kernel      per CTA R q-block rows of one head: pooled logits, row
+//                      softmax, hybrid selection.  Launched while the pooling
+//                      drains; it waits for the pooling's results.
+//   csc_split_kernel   (when the column lists are wanted) per CTA one head and
+//                      32 kv-blocks: the ascending lists of q-blocks, the row
+//                      range split across 8 warps.
+// A dependent kernel only launches once every CTA of the previous one has
+// started, so its waiting CTAs never keep the previous kernel from running.
+constexpr int kSelkThreads = 256;                   // 8 warps, one row each
+#ifndef SPARGE_SELK_MINB
+#define SPARGE_SELK_MINB 3
+#endif
+constexpr int kSelkRows = kSelkThreads / 32;        // q-blocks per CTA (max)
+constexpr int kSelkLogitFloats = 10240;             // 40 KB of logits per CTA
+
+struct SelkSmem {
+  uint32_t hcnt[kSelkRows][256];                    // radix fallback (Mk > 2048)
+  unsigned long long hsum[kSelkRows][256];
+};
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSelkThreads, SPARGE_SELK_MINB) select_kernel(
+    const float* __restrict__ qbar, const float* __restrict__ kbarT, int Mq, int Mk, int Mkw,
+    int R, float scale, int ktop, float p, uint32_t* __restrict__ bitmask,
+    int32_t* __restrict__ row_idx, int32_t* __restrict__ row_cnt, float* __restrict__ logit_out,
+    float* __restrict__ prob_out) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  SelkSmem* hs = reinterpret_cast<SelkSmem*>(smem);
+  float* qs = reinterpret_cast<float*>(smem + sizeof(SelkSmem));  // [D][kSelkRows]
+  float* ls = qs + kSelkRows * D;                                 // [R][Mk]
+  const int nrb = (Mq + R - 1) / R;
+  const int bh = blockIdx.x / nrb;
+  const int i0 = (blockIdx.x % nrb) * R;
+  const int nrows = min(R, Mq - i0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_wait_primary();  // pooled means are complete and visible
+  pdl_launch_dependents();
+
+  // q rows stored transposed, qs[c * 8 + r], so one pair of 16-byte
+  // broadcast reads gives channel c of all eight rows.
+  const float* qsrc = qbar + ((long long)bh * Mq + i0) * D;
+  for (int t = threadIdx.x; t < kSelkRows * D; t += kSelkThreads) {
+    const int r = t / D, c = t % D;
+    qs[c * kSelkRows + r] = (r < nrows) ? __ldcg(qsrc + t) : 0.f;
+  }
+  __syncthreads();
+
+  // Pooled logits from the transposed K means kbarT[bh][c][j]: a warp reads
+  // 32 consecutive kv-blocks of one channel (one 128-byte line); each thread
+  // carries two columns so that 2 x 16 loads are in flight.  (Wider tiles
+  // per thread leave fewer loads in flight; the phase is bound by L2 latency
+  // and the FMA rate, about 5.6 us of FMA work per SM at the 480p shape.)
+  static_assert(kSelkRows == 8, "two float4 reads cover the q rows");
+  const float* kt = kbarT + (long long)bh * D * Mk;
+  for (int j0 = threadIdx.x; j0 < Mk; j0 += 2 * kSelkThreads) {
+    const int j1 = j0 + kSelkThreads;
+    const bool has1 = j1 < Mk;
+    float a0[kSelkRows], a1[kSelkRows];
+#pragma unroll
+    for (int r = 0; r < kSelkRows; ++r) a0[r] = a1[r] = 0.f;
+#pragma unroll 16
+    for (int c = 0; c < D; ++c) {
+      const float k0 = __ldcg(kt + (long long)c * Mk + j0);
+      const float k1 = has1 ? __ldcg(kt + (long long)c * Mk + j1) : 0.f;
+      const float4 qa = *reinterpret_cast<const float4*>(qs + c * kSelkRows);
+      const float4 qb = *reinterpret_cast<const float4*>(qs + c * kSelkRows + 4);
+      const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+      for (int r = 0; r < kSelkRows; ++r) {
+        a0[r] = fmaf(qv[r], k0, a0[r]);
+        a1[r] = fmaf(qv[r], k1, a1[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kSelkRows; ++r) {
+      if (r < nrows) {
+        ls[r * Mk + j0] = a0[r] * scale;
+        if (has1) ls[r * Mk + j1] = a1[r] * scale;
+      }
+    }
+  }
+  __syncthreads();
+
+  if (warp < nrows) {
+    float* row = ls + warp * Mk;
+    const long long grow = (long long)bh * Mq + i0 + warp;
+    float m = -INFINITY;
+    for (int j = lane; j < Mk; j += 32) m = fmaxf(m, row[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    float sum = 0.f;
+    for (int j = lane; j < Mk; j += 32) {
+      const float lg = row[j];
+      if (logit_out) logit_out[grow * Mk + j] = lg;
+      const float e = expf(lg - m);
+      row[j] = e;
+      sum += e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    for (int j = lane; j < Mk; j += 32) {
+      const float pj = __fdiv_rn(row[j], sum);
+      row[j] = pj;
+      if (prob_out) prob_out[grow * Mk + j] = pj;
+    }
+    __syncwarp();
+    select_row_any(row, Mk, ktop, p, hs->hcnt[warp], hs->hsum[warp], bitmask + grow * Mkw,
+                   row_idx + grow * Mk, row_cnt + grow);
+  }
+}
+
+// CTA = (head, bitmask word w), 8 warps.  Warp g scans rows [g*Mq/8, (g+1)*Mq/8)
+// of kv-blocks 32w + lane, counts them, and after a prefix over the warps
+// writes its q-block indices at their ascending positions.
+constexpr int kCscSplitThreads = 256;
+__global__ void __launch_bounds__(kCscSplitThreads) csc_split_kernel(
+    const uint32_t* __restrict__ bitmask, int Mq, int Mk, int Mkw, int32_t* __restrict__ col_idx,
+    int32_t* __restrict__ col_cnt) {
+  extern __shared__ uint32_t words[];  // [Mq]
+  __shared__ int cnt_w[8][32];
+  pdl_wait_primary();
+  const int bh = blockIdx.x / Mkw;
+  const int w = blockIdx.x % Mkw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t* src = bitmask + (long long)bh * Mq * Mkw + w;
+  for (int i = threadIdx.x; i < Mq; i += kCscSplitThreads)
+    words[i] = __ldcg(src + (long long)i * Mkw);
+  __syncthreads();
+  const int per = (Mq + 7) / 8;
+  const int lo = min(Mq, warp * per), hi = min(Mq, lo + per);
+  int cnt = 0;
+  for (int i = lo; i < hi; ++i) cnt += (words[i] >> lane) & 1u;
+  cnt_w[warp][lane] = cnt;
+  __syncthreads();
+  int off = 0, total = 0;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int c = cnt_w[g][lane];
+    off += g < warp ? c : 0;
+    total += c;
+  }
+  const int j = w * 32 + lane;
+  if (j < Mk) {
+    int32_t* out = col_idx + ((long long)bh * Mk + j) * Mq + off;
+    for (int i = lo; i < hi; ++i)
+      if ((words[i] >> lane) & 1u) *out++ = i;
+    if (warp == 0) col_cnt[(long long)bh * Mk + j] = total;
+  }
 }
 
 }  // namespace
@@ -404,46 +651,19 @@ int select_rows_per_cta(int Mk) {
 }
 
 cudaError_t launch_pool(const Geom& g, const void* q, const void* k, float* qbar, float* kbar,
-                        float* kbarT, cudaStream_t st) {
+                        cudaStream_t st) {
   const int do_q = qbar != nullptr;
-  const int do_k = (kbar != nullptr) || (kbarT != nullptr);
+  const int do_k = kbar != nullptr;
   const long long units = (do_q ? (long long)g.BH * g.Mq : 0) + (do_k ? (long long)g.BH * g.Mk : 0);
   if (units == 0) return cudaSuccess;
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   const auto* kk = static_cast<const __nv_bfloat16*>(k);
   if (g.d == 128)
     pool_kernel<128><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
-        qq, kk, g.BH, g.N, g.bq, g.bk, g.Mq, g.Mk, do_q, do_k, qbar, kbar, kbarT);
+        qq, kk, g.BH, g.N, g.bq, g.bk, g.Mq, g.Mk, do_q, qbar, kbar, nullptr);
   else
     pool_kernel<64><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
-        qq, kk, g.BH, g.N, g.bq, g.bk, g.Mq, g.Mk, do_q, do_k, qbar, kbar, kbarT);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_score_select(const Geom& g, const float* qbar, const float* kbarT, float scale,
-                                int ktop, float p, uint32_t* bitmask, int32_t* row_idx,
-                                int32_t* row_cnt, float* logit_out, float* prob_out,
-                                cudaStream_t st) {
-  const int R = select_rows_per_cta(g.Mk);
-  const int nrb = (g.Mq + R - 1) / R;
-  const size_t smem = select_smem_bytes(g.d, R, g.Mk);
-  const unsigned grid = static_cast<unsigned>((long long)g.BH * nrb);
-  cudaError_t e;
-  if (g.d == 128) {
-    e = cudaFuncSetAttribute(score_select_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    score_select_kernel<128><<<grid, kSelThreads, smem, st>>>(qbar, kbarT, g.Mq, g.Mk, g.Mkw, R,
-                                                               scale, ktop, p, bitmask, row_idx,
-                                                               row_cnt, logit_out, prob_out);
-  } else {
-    e = cudaFuncSetAttribute(score_select_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    score_select_kernel<64><<<grid, kSelThreads, smem, st>>>(qbar, kbarT, g.Mq, g.Mk, g.Mkw, R,
-                                                              scale, ktop, p, bitmask, row_idx,
-                                                              row_cnt, logit_out, prob_out);
-  }
+        qq, kk, g.BH, g.N, g.bq, g.bk, g.Mq, g.Mk, do_q, qbar, kbar, nullptr);
   return cudaGetLastError();
 }
 
@@ -468,6 +688,68 @@ cudaError_t launch_csc(const Geom& g, const uint32_t* bitmask, int32_t* col_idx,
   csc_kernel<<<static_cast<unsigned>((long long)g.BH * g.Mkw), kCscThreads, smem, st>>>(
       bitmask, g.Mq, g.Mk, g.Mkw, col_idx, col_cnt);
   return cudaGetLastError();
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int D>
+cudaError_t launch_mask_pipeline_impl(const Geom& g, const void* q, const void* k, float* qbar,
+                                      float* kbarT, float scale, int ktop, float p,
+                                      uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
+                                      int32_t* col_idx, int32_t* col_cnt, float* logit_out,
+                                      float* prob_out, cudaStream_t st) {
+  const long long units = (long long)g.BH * (g.Mq + g.Mk);
+  pool_kernel<D><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g.BH, g.N, g.bq,
+      g.bk, g.Mq, g.Mk, 1, qbar, nullptr, kbarT);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int R = kSelkLogitFloats / g.Mk;
+  R = R < 1 ? 1 : (R > kSelkRows ? kSelkRows : R);
+  const int nrb = (g.Mq + R - 1) / R;
+  const size_t smem = sizeof(SelkSmem) + (size_t)kSelkRows * D * sizeof(float) +
+                      (size_t)R * g.Mk * sizeof(float);
+  if ((e = cudaFuncSetAttribute(select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem))) != cudaSuccess)
+    return e;
+  if ((e = launch_pdl(select_kernel<D>, static_cast<unsigned>((long long)g.BH * nrb),
+                      kSelkThreads, smem, st, static_cast<const float*>(qbar),
+                      static_cast<const float*>(kbarT), g.Mq, g.Mk, g.Mkw, R, scale, ktop, p,
+                      bitmask, row_idx, row_cnt, logit_out, prob_out)) != cudaSuccess)
+    return e;
+  if (col_idx != nullptr) {
+    e = launch_pdl(csc_split_kernel, static_cast<unsigned>((long long)g.BH * g.Mkw),
+                   kCscSplitThreads, (size_t)g.Mq * sizeof(uint32_t), st,
+                   static_cast<const uint32_t*>(bitmask), g.Mq, g.Mk, g.Mkw, col_idx, col_cnt);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mask_pipeline(const Geom& g, const void* q, const void* k, float* qbar,
+                                 float* kbarT, float scale, int ktop, float p, uint32_t* bitmask,
+                                 int32_t* row_idx, int32_t* row_cnt, int32_t* col_idx,
+                                 int32_t* col_cnt, float* logit_out, float* prob_out,
+                                 cudaStream_t st) {
+  if (g.d == 128)
+    return launch_mask_pipeline_impl<128>(g, q, k, qbar, kbarT, scale, ktop, p, bitmask, row_idx,
+                                          row_cnt, col_idx, col_cnt, logit_out, prob_out, st);
+  return launch_mask_pipeline_impl<64>(g, q, k, qbar, kbarT, scale, ktop, p, bitmask, row_idx,
+                                       row_cnt, col_idx, col_cnt, logit_out, prob_out, st);
 }
 
 }  // namespace sparge

@@ -67,7 +67,7 @@ extern "C" int sparge_mask_noalloc(const sparge_shape* shape, const void* q, con
   void* scratch = nullptr;
   const int rs = sparge::scratch_address(&scratch);
   if (rs != SPARGE_OK) return rs;
-  // The pooling kernel overwrites every scratch byte the selection reads, so
+  // The pooling kernels overwrite every scratch byte the selection reads, so
   // nothing has to be cleared between calls.
   return sparge_mask(shape, q, k, k_frac, p, softmax_scale, bitmask, row_idx, row_cnt, col_idx,
                      col_cnt, pooled_logit, pooled_prob, scratch, sparge::kNoAllocScratchBytes,

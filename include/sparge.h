@@ -104,8 +104,13 @@ int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes);
  *                  set; needed by sparge_attn_bwd.
  *   pooled_logit : fp32 [B,H,Mq,Mk] out, L (nullable).
  *   pooled_prob  : fp32 [B,H,Mq,Mk] out, P (nullable).
- *   workspace    : device buffer of sparge_mask_workspace_bytes bytes.
- * The mask is a deterministic function of the fp32 P it computes.
+ *   workspace    : device buffer of sparge_mask_workspace_bytes bytes (pooled
+ *                  Q and K; no initial contents needed).
+ *   status       : nullable; unused (the mask kernels have no internal waits).
+ * The mask is a deterministic function of the fp32 P it computes.  The call
+ * launches three kernels (two without the column lists) chained by
+ * programmatic dependent launch: pooling, then pooled map and selection,
+ * then the column lists.
  */
 int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k_frac, float p,
                 float softmax_scale, uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
