@@ -276,6 +276,8 @@ __global__ void __launch_bounds__(kGradThreads, 1)
     // S_t = Q_t K^T and dP_t = dO_t V^T (M = 128 query rows, N = 64 keys).
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+      const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(s0 + C::off_v, 16, 1024);
       bool ok = mbar_wait(bar(C::B_KV), 0, kWaitTimeoutNs);
       for (int t = 0; ok && t < n; ++t) {
         const int s = t % C::NST;
@@ -287,22 +289,20 @@ __global__ void __launch_bounds__(kGradThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t qb = s0 + C::off_q + s * C::kQ;
-        const uint32_t ob = s0 + C::off_do + s * C::kQ;
+        const uint64_t dq = sdesc_sw128(s0 + C::off_q + s * C::kQ, 16, 1024);
+        const uint64_t ddo = sdesc_sw128(s0 + C::off_do + s * C::kQ, 16, 1024);
         const uint32_t dS = tmem + (t & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
           const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16(dS, sdesc_sw128(qb + ko, 16, 1024),
-                      sdesc_sw128(s0 + C::off_k + kko, 16, 1024), idS, kk > 0);
+          tc_mma_bf16(dS, sdesc_add(dq, ko), sdesc_add(dk0, kko), idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
           const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16(dS + 64, sdesc_sw128(ob + ko, 16, 1024),
-                      sdesc_sw128(s0 + C::off_v + kko, 16, 1024), idS, kk > 0);
+          tc_mma_bf16(dS + 64, sdesc_add(ddo, ko), sdesc_add(dv0, kko), idS, kk > 0);
         }
         tc_commit(bar(C::B_SF + (t & 1)));
       }
@@ -324,19 +324,17 @@ __global__ void __launch_bounds__(kGradThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t qb = s0 + C::off_q + su * C::kQ;
-        const uint32_t ob = s0 + C::off_do + su * C::kQ;
-        const uint32_t pbuf = s0 + C::off_p + pb * C::kP;
-        const uint32_t dsbuf = s0 + C::off_ds + pb * C::kP;
+        const uint64_t dq = sdesc_sw128(s0 + C::off_q + su * C::kQ, kBM * 128, 1024);
+        const uint64_t ddo = sdesc_sw128(s0 + C::off_do + su * C::kQ, kBM * 128, 1024);
+        const uint64_t dpb = sdesc_sw128(s0 + C::off_p + pb * C::kP, kBM * 128, 1024);
+        const uint64_t dsb = sdesc_sw128(s0 + C::off_ds + pb * C::kP, kBM * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          tc_mma_bf16(tmem + C::col_dv, sdesc_sw128(ob + kk * 2048, kBM * 128, 1024),
-                      sdesc_sw128(pbuf + kk * 2048, kBM * 128, 1024), idG,
+          tc_mma_bf16(tmem + C::col_dv, sdesc_add(ddo, kk * 2048), sdesc_add(dpb, kk * 2048), idG,
                       (u > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kBM / 16; ++kk)
-          tc_mma_bf16(tmem + C::col_dk, sdesc_sw128(qb + kk * 2048, kBM * 128, 1024),
-                      sdesc_sw128(dsbuf + kk * 2048, kBM * 128, 1024), idG,
+          tc_mma_bf16(tmem + C::col_dk, sdesc_add(dq, kk * 2048), sdesc_add(dsb, kk * 2048), idG,
                       (u > 0 || kk > 0) ? 1u : 0u);
         // S/dP(u) completed before P/dS(u) were written, so the Q/dO stage is
         // free once these MMAs complete.
@@ -561,6 +559,8 @@ __global__ void __launch_bounds__(kGradThreads, 1)
     // S_t = Q K_t^T and dP_t = dO V_t^T.
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+      const uint64_t dq0 = sdesc_sw128(s0 + C::off_q, 16, 1024);
+      const uint64_t ddo0 = sdesc_sw128(s0 + C::off_do, 16, 1024);
       bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
       for (int t = 0; ok && t < n; ++t) {
         const int s = t % C::NST;
@@ -573,12 +573,13 @@ __global__ void __launch_bounds__(kGradThreads, 1)
           break;
         }
         tc_fence_after();
+        const uint64_t dk = sdesc_sw128(s0 + C::off_k + s * C::kKV, 16, 1024);
+        const uint64_t dv = sdesc_sw128(s0 + C::off_v + s * C::kKV, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
           const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16(dS, sdesc_sw128(s0 + C::off_q + ko, 16, 1024),
-                      sdesc_sw128(s0 + C::off_k + s * C::kKV + kko, 16, 1024), idS, kk > 0);
+          tc_mma_bf16(dS, sdesc_add(dq0, ko), sdesc_add(dk, kko), idS, kk > 0);
         }
         if (!mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
           ok = false;
@@ -589,8 +590,7 @@ __global__ void __launch_bounds__(kGradThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
           const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16(dS + 64, sdesc_sw128(s0 + C::off_do + ko, 16, 1024),
-                      sdesc_sw128(s0 + C::off_v + s * C::kKV + kko, 16, 1024), idS, kk > 0);
+          tc_mma_bf16(dS + 64, sdesc_add(ddo0, ko), sdesc_add(dv, kko), idS, kk > 0);
         }
         tc_commit(bar(C::B_SF + (t & 1)));
       }
@@ -610,12 +610,11 @@ __global__ void __launch_bounds__(kGradThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t dsb = C::ds_addr(s0, u);
-        const uint32_t kb = s0 + C::off_k + su * C::kKV;
+        const uint64_t dds = sdesc_sw128(C::ds_addr(s0, u), 16, 1024);
+        const uint64_t dk = sdesc_sw128(s0 + C::off_k + su * C::kKV, kBN * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc_mma_bf16(tmem + C::col_dq, sdesc_sw128(dsb + kk * 32, 16, 1024),
-                      sdesc_sw128(kb + kk * 2048, kBN * 128, 1024), idQ,
+          tc_mma_bf16(tmem + C::col_dq, sdesc_add(dds, kk * 32), sdesc_add(dk, kk * 2048), idQ,
                       (u > 0 || kk > 0) ? 1u : 0u);
         // S/dP(u) completed before dS(u) was written, so stage su is free
         // once this MMA completes.

@@ -11,22 +11,24 @@
 // list of kept 64-token kv-blocks; two CTAs share an SM so that one CTA's
 // latencies (barrier hand-offs, loads, its prologue and epilogue) overlap the
 // other's work.  Warp roles (224 threads):
-//   warp 4   TMA producer: Q once, then K_j / V_j into a 2-stage ring.
+//   warp 4   TMA producer: Q once, then K_j / V_j into a 2-stage ring; a
+//            K slot is reloaded once S of its tile has completed, a V slot
+//            once PV of its tile has.
 //   warp 5   S issuer: S_t = Q K_t^T into a double-buffered TMEM tile
 //            (128 x 64 fp32).
-//   warp 6   PV issuer: O += P_t V_t into a TMEM accumulator (128 x d fp32).
-//            Separate issuing warps let the S and PV MMAs of neighbouring
-//            tiles overlap (a 128 x 64 x 16 MMA occupies the tensor pipe for
-//            about 48 cycles on this GPU).
+//   warp 6   PV issuer: O += P_t V_t into a TMEM accumulator (128 x d fp32),
+//            with the A operand P_t read from tensor memory.  Separate issuing
+//            warps let the S and PV MMAs of neighbouring tiles overlap.
 //   warps 0-3 softmax: thread r owns query row r (= TMEM lane r).  It reads
 //            S_t, masks the ragged kv tail, keeps the running max m and sum l
-//            in base 2 and writes P_t (bf16) into shared memory in the
-//            128-byte-swizzled K-major layout the PV MMA reads.  With d = 128
-//            P_t goes into the K half of tile t's own stage: K_t is dead once
-//            S_t has completed, and the stage is not reloaded before PV_t
-//            completes.  O is rescaled in TMEM only when the running max
-//            grows by more than 8 (a factor 256); below that the stale max
-//            stays exact because l and O share it.  Finally O is scaled by 1/l.
+//            in base 2 and writes P_t (bf16 pairs) over the first 32 columns
+//            of S_t's own TMEM tile, where the PV MMA reads it.  Keeping P out
+//            of shared memory leaves the shared-memory bandwidth (128 B per
+//            clock per SM, which the 128 x 64 x 16 MMAs with both operands in
+//            shared memory already use in full) to the operands and loads.
+//            O is rescaled in TMEM only when the running max grows by more
+//            than 8 (a factor 256); below that the stale max stays exact
+//            because l and O share it.  Finally O is scaled by 1/l.
 // Every barrier wait is bounded; a timeout records SPARGE_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -54,24 +56,21 @@ constexpr float kRescaleLog2 = 8.0f;
 template <int D>
 struct FwdCfg {
   static constexpr int NST = 2;                       // K/V stages
-  static constexpr int NP = 2;                        // P phases (buffers when separate)
+  static constexpr int NP = 2;                        // P phases (the S/P TMEM tiles)
   static constexpr int KCH = D / 64;                  // 128-byte chunks per row
   static constexpr uint32_t kQ = kBM * D * 2;
   static constexpr uint32_t kKV = kBN * D * 2;
-  static constexpr uint32_t kP = kBM * kBN * 2;
-  // P_t lives in tile t's K stage when that stage is large enough (d = 128).
-  static constexpr bool P_IN_K = kKV >= kP;
   static constexpr uint32_t off_q = 0;
   static constexpr uint32_t off_k = off_q + kQ;
   static constexpr uint32_t off_v = off_k + NST * kKV;
-  static constexpr uint32_t off_p = off_v + NST * kKV;
-  static constexpr uint32_t off_bar = off_p + (P_IN_K ? 0 : NP * kP);
+  static constexpr uint32_t off_bar = off_v + NST * kKV;
   // barriers
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;
   static constexpr int B_VF = B_KF + NST;
-  static constexpr int B_KE = B_VF + NST;
-  static constexpr int B_SF = B_KE + NST;
+  static constexpr int B_KE = B_VF + NST;   // K slot free (S of its tile done)
+  static constexpr int B_VE = B_KE + NST;   // V slot free (PV of its tile done)
+  static constexpr int B_SF = B_VE + NST;
   static constexpr int B_PF = B_SF + 2;     // count 128 (all softmax threads)
   static constexpr int B_PV = B_PF + NP;
   static constexpr int B_DRAIN = B_PV + 2;  // count 2 (both issuers)
@@ -79,16 +78,23 @@ struct FwdCfg {
   static constexpr uint32_t off_tmem_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_tmem_slot + 16;
   static constexpr uint32_t smem_alloc = bytes + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t tmem_cols = 256;            // S0 [0,64) S1 [64,128) O [128,128+D)
+  // S0 [0,64) S1 [64,128) O [128,128+D); P_t (bf16 pairs) over the first 32
+  // columns of S_(t & 1).
+  static constexpr uint32_t tmem_cols = 256;
   static constexpr uint32_t col_s = 0;
   static constexpr uint32_t col_o = 128;
 };
 
-// Shared-memory address of P_t.
-template <int D>
-__device__ __forceinline__ uint32_t p_tile_addr(uint32_t s0, int t) {
-  using C = FwdCfg<D>;
-  return C::P_IN_K ? s0 + C::off_k + (t % C::NST) * C::kKV : s0 + C::off_p + (t % C::NP) * C::kP;
+// tcgen05.mma kind::f16 with the A operand in tensor memory (M lanes, K/2
+// 32-bit columns holding bf16 pairs, element 2c in the low half of column c).
+__device__ __forceinline__ void tc_mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 template <int D>
@@ -153,6 +159,10 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(s0 + C::off_k + s * C::kKV + c * kBN * 128, &tmK, bar(C::B_KF + s), c * 64,
                       j * kBN, bh);
+        if (t >= C::NST && !mbar_wait(bar(C::B_VE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+          report_error(status, SPARGE_ERR_TIMEOUT);
+          break;
+        }
         mbar_arrive_expect_tx(bar(C::B_VF + s), C::kKV);
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(s0 + C::off_v + s * C::kKV + c * kBN * 128, &tmV, bar(C::B_VF + s), c * 64,
@@ -170,28 +180,28 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
     // ------------------------------------------------------------ S issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
+      const uint64_t dq0 = sdesc_sw128(s0 + C::off_q, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
       bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
       for (int t = 0; ok && t < n; ++t) {
         const int s = t % C::NST;
-        // S buffer t & 1 was last read by the softmax of tile t - 2, which
-        // finished reading it before P(t - 2) became full.
+        // TMEM tile t & 1 holds P(t - 2) until PV(t - 2) has completed.
         if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs) ||
-            (t >= 2 &&
-             !mbar_wait(bar(C::B_PF + (t % C::NP)), ((t - 2) / C::NP) & 1, kWaitTimeoutNs))) {
+            (t >= 2 && !mbar_wait(bar(C::B_PV + (t & 1)), ((t - 2) >> 1) & 1, kWaitTimeoutNs))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t kbase = s0 + C::off_k + s * C::kKV;
+        const uint64_t dk = sdesc_add(dk0, s * C::kKV);
         const uint32_t dS = tmem + C::col_s + (t & 1) * kBN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(s0 + C::off_q + (kk >> 2) * (kBM * 128) + koff, 16, 1024);
-          const uint64_t b = sdesc_sw128(kbase + (kk >> 2) * (kBN * 128) + koff, 16, 1024);
-          tc_mma_bf16(dS, a, b, idS, kk > 0);
+          tc_mma_bf16(dS, sdesc_add(dq0, (kk >> 2) * (kBM * 128) + koff),
+                      sdesc_add(dk, (kk >> 2) * (kBN * 128) + koff), idS, kk > 0);
         }
         tc_commit(bar(C::B_SF + (t & 1)));
+        tc_commit(bar(C::B_KE + s));
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       // Drain: every MMA this thread issued has completed once this arrives.
@@ -211,17 +221,13 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
           break;
         }
         tc_fence_after();
-        const uint32_t pbase = p_tile_addr<D>(s0, u);
-        const uint32_t vbase = s0 + C::off_v + su * C::kKV;
+        const uint32_t ap = tmem + C::col_s + (u & 1) * kBN;
+        const uint64_t dv = sdesc_sw128(s0 + C::off_v + su * C::kKV, kBN * 128, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(pbase + kk * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024);
-          tc_mma_bf16(tmem + C::col_o, a, b, idO, (u > 0 || kk > 0) ? 1u : 0u);
-        }
-        // S(u) completed before P(u) was written, so stage su (K and V) is free
-        // once this PV completes.
-        tc_commit(bar(C::B_KE + su));
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          tc_mma_bf16_tmem_a(tmem + C::col_o, ap + kk * 8, sdesc_add(dv, kk * 16 * 128), idO,
+                             (u > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(C::B_VE + su));
         tc_commit(bar(C::B_PV + (u & 1)));
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
@@ -319,19 +325,12 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
           m_used = m_new;
         }
       }
-      // A separate P buffer t % NP is free once PV(t - NP) has completed; P in
-      // the K stage needs no wait (the stage held K_t, already consumed).
-      if (!C::P_IN_K && t >= C::NP) {
-        const int u = t - C::NP;
-        if (!warp_wait(bar(C::B_PV + (u & 1)), (u >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-      }
-      uint8_t* prow = sm + (p_tile_addr<D>(s0, t) - s0);
+      // P_t over the first 32 columns of S_t's tile (this thread's S_t row
+      // is already in registers).
       float rs8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
+      uint32_t pk[32];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         float p[8];
@@ -340,15 +339,18 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
           p[e] = ex2_approx(fmaf(x[ch * 8 + e], scale_log2, -m_used));
           rs8[e] += p[e];
         }
-        uint4 v;
-        v.x = pack_bf16x2(p[0], p[1]);
-        v.y = pack_bf16x2(p[2], p[3]);
-        v.z = pack_bf16x2(p[4], p[5]);
-        v.w = pack_bf16x2(p[6], p[7]);
-        *reinterpret_cast<uint4*>(prow + sw128_offset(r, ch * 16)) = v;
+        pk[ch * 4 + 0] = pack_bf16x2(p[0], p[1]);
+        pk[ch * 4 + 1] = pack_bf16x2(p[2], p[3]);
+        pk[ch * 4 + 2] = pack_bf16x2(p[4], p[5]);
+        pk[ch * 4 + 3] = pack_bf16x2(p[6], p[7]);
       }
       l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-      fence_proxy_async_smem();
+      {
+        const uint32_t pa = lane_base + C::col_s + (t & 1) * kBN;
+        SPARGE_TMEM_ST_X16(pa, pk);
+        SPARGE_TMEM_ST_X16(pa + 16, (pk + 16));
+        tmem_st_wait();
+      }
       tc_fence_before();
       mbar_arrive(bar(C::B_PF + (t % C::NP)));
     }

@@ -164,6 +164,15 @@ SPARGE_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// Moves a shared-memory descriptor's start address by `bytes` (a multiple of
+// 16).  Shared addresses stay below 2^18, so the 14-bit field cannot carry.
+// Issue loops add constant offsets to a base descriptor built once per tile:
+// rebuilding both descriptors per MMA costs about 63 cycles of issue per
+// 128 x 64 x 16 MMA on sm_103a, more than the 48 the tensor pipe needs.
+SPARGE_DEV uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Byte offset of element (row, col) of a bf16 tile stored as 128-byte rows with
 // the 128-byte swizzle (16-byte chunk index XOR row % 8); tile base 1024-aligned.
 SPARGE_DEV uint32_t sw128_offset(uint32_t row, uint32_t col_bytes) {
