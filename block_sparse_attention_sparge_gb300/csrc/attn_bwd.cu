@@ -19,7 +19,8 @@
 //                     dO, Q, P and dS read in the MN-major smem layout.
 //   bwd_dq_kernel     one CTA per q-block, loops over its kept kv-blocks (CSR
 //                     list); recomputes S, dP and dS and accumulates
-//                     dQ += dS K in TMEM.
+//                     dQ += dS K in TMEM.  Q and dO (reused by every tile)
+//                     and dS are MMA A operands read from TMEM.
 // Roles per CTA: eight compute warps (two per TMEM lane quarter, each owning
 // 32 of a tile's 64 key columns), a TMA producer warp and two MMA-issuing
 // warps (S and dP; then the gradient MMAs).  Every wait is bounded.
@@ -69,64 +70,57 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 }
 
 // ---------------------------------------------------------------- work order
-// Longest-first launch order: writes order[pos] = item for items [0, n) sorted
-// by count descending (a counting sort; equal counts in any order).  Launching
-// the longest lists first keeps a few long lists (attention-sink blocks that
-// every q-block keeps) from running alone at the end of the grid.
+// Launch order of the gradient CTAs: the lists longer than twice the mean
+// first, then the others, each group in index order (a stable partition).
+// Long lists (attention-sink blocks that nearly every q-block keeps) would
+// otherwise run alone at the end of the grid; index order keeps the CTAs of
+// one head together, so that head's Q/dO (or K/V) tiles are served from L2.
 constexpr int kOrderThreads = 1024;
 __global__ void __launch_bounds__(kOrderThreads) order_by_count_kernel(
-    const int32_t* __restrict__ cnt, int n, int max_cnt, int32_t* __restrict__ order) {
-  extern __shared__ int32_t start[];  // [max_cnt + 1], indexed by count
-  __shared__ int32_t warp_tot[kOrderThreads / 32];
+    const int32_t* __restrict__ cnt, int n, int32_t* __restrict__ order) {
+  __shared__ long long red[kOrderThreads / 32];
+  __shared__ int scan[kOrderThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int nb = max_cnt + 1;
-  for (int b = tid; b < nb; b += kOrderThreads) start[b] = 0;
+  const int E = (n + kOrderThreads - 1) / kOrderThreads;
+  const int lo = min(n, tid * E), hi = min(n, lo + E);
+  // Total of the counts.
+  long long sum = 0;
+  for (int it = lo; it < hi; ++it) sum += max(__ldg(cnt + it), 0);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) red[w] = sum;
   __syncthreads();
-  for (int it = tid; it < n; it += kOrderThreads)
-    atomicAdd(&start[min(max(__ldg(cnt + it), 0), max_cnt)], 1);
-  __syncthreads();
-  // Exclusive scan over counts in descending order: thread t owns the run of
-  // E reversed positions [t*E, t*E + E), position r meaning count max_cnt - r.
-  const int E = (nb + kOrderThreads - 1) / kOrderThreads;
-  int local = 0;
-  for (int e = 0; e < E; ++e) {
-    const int r = tid * E + e;
-    if (r < nb) local += start[max_cnt - r];
-  }
-  int incl = local;
+  long long total = 0;
+#pragma unroll 4
+  for (int i = 0; i < kOrderThreads / 32; ++i) total += red[i];
+  // Item `it` is long when cnt * n > 2 * total.
+  auto is_long = [&](int it) { return (long long)max(__ldg(cnt + it), 0) * n > 2 * total; };
+  int nl = 0;
+  for (int it = lo; it < hi; ++it) nl += is_long(it) ? 1 : 0;
+  // Exclusive scan of the per-thread long counts.
+  int incl = nl;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
-  if (lane == 31) warp_tot[w] = incl;
+  if (lane == 31) scan[w] = incl;
   __syncthreads();
   if (w == 0) {
-    int t = warp_tot[lane];
+    int t = scan[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, t, o);
       if (lane >= o) t += v;
     }
-    warp_tot[lane] = t;  // inclusive warp totals
+    scan[lane] = t;  // inclusive warp totals
   }
   __syncthreads();
-  int run = incl - local + (w > 0 ? warp_tot[w - 1] : 0);
-  __syncthreads();  // every thread has read its histogram run
-  for (int e = 0; e < E; ++e) {
-    const int r = tid * E + e;
-    if (r < nb) {
-      const int c = max_cnt - r;
-      const int h = start[c];
-      start[c] = run;
-      run += h;
-    }
-  }
-  __syncthreads();
-  for (int it = tid; it < n; it += kOrderThreads) {
-    const int pos = atomicAdd(&start[min(max(__ldg(cnt + it), 0), max_cnt)], 1);
-    order[pos] = it;
-  }
+  const int before_long = incl - nl + (w > 0 ? scan[w - 1] : 0);
+  const int n_long = scan[kOrderThreads / 32 - 1];
+  int pl = before_long;            // next long position
+  int ps = n_long + lo - before_long;  // next short position
+  for (int it = lo; it < hi; ++it) order[is_long(it) ? pl++ : ps++] = it;
 }
 
 // Writes 32 bf16 values (half of a 128-byte row: 16-byte chunks 4h .. 4h+3)
@@ -453,35 +447,72 @@ struct DqCfg {
   static constexpr int KCH = D / 64;
   static constexpr uint32_t kKV = kBN * D * 2;
   static constexpr uint32_t kQ = kBM * D * 2;
-  static constexpr uint32_t kP = kBM * kBN * 2;
-  // With d = 128, dS_t goes into the V tile of its own stage (V_t is dead once
-  // dP_t has completed; the stage is not reloaded before dQ_t completes).
-  static constexpr bool DS_IN_V = kKV >= kP;
-  static constexpr int NST = DS_IN_V ? 4 : 3;
+  static constexpr int NST = 4;
   static constexpr uint32_t off_q = 0;
   static constexpr uint32_t off_do = off_q + kQ;
   static constexpr uint32_t off_k = off_do + kQ;
   static constexpr uint32_t off_v = off_k + NST * kKV;
-  static constexpr uint32_t off_ds = off_v + NST * kKV;  // 2 buffers unless DS_IN_V
-  static constexpr uint32_t off_bar = off_ds + (DS_IN_V ? 0 : 2 * kP);
+  static constexpr uint32_t off_bar = off_v + NST * kKV;
   static constexpr int B_Q = 0;
-  static constexpr int B_KF = 1;
+  static constexpr int B_QT = 1;            // Q, dO copied into TMEM (count 256)
+  static constexpr int B_KF = 2;
   static constexpr int B_VF = B_KF + NST;
-  static constexpr int B_KE = B_VF + NST;
-  static constexpr int B_SF = B_KE + NST;   // 2
-  static constexpr int B_DSF = B_SF + 2;    // 2, count 256
-  static constexpr int B_DSE = B_DSF + 2;   // 2
+  static constexpr int B_KE = B_VF + NST;   // K slot free (dQ of its tile done)
+  static constexpr int B_VE = B_KE + NST;   // V slot free (dP of its tile done)
+  static constexpr int B_SF = B_VE + NST;   // 2
+  static constexpr int B_DSF = B_SF + 2;    // 2, count 256 (dS written)
+  static constexpr int B_DSE = B_DSF + 2;   // 2 (dQ of the tile done: TMEM tile free)
   static constexpr int B_DONE = B_DSE + 2;  // count 2
   static constexpr int NBAR = B_DONE + 1;
   static constexpr uint32_t off_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_slot + 16;
   static constexpr uint32_t smem_alloc = bytes + 1024;
-  static constexpr uint32_t tmem_cols = 512;  // S/dP x2 [0,256), dQ [256, 256+D)
+  // TMEM: S/dP x2 [0,256) (S_b at 128b, dP_b at 128b + 64), dQ [256, 256+D),
+  // Q and dO as MMA A operands (bf16 pairs, D/2 columns each) after it.  dS_t
+  // (bf16 pairs, 32 columns) goes over columns 16..47 of S_t's tile: the half
+  // of a row that read S columns 0..31 writes 16..31, the other 32..47, so no
+  // warp overwrites columns another warp has still to read.  Q and dO in TMEM
+  // keep their operand reads (reused by every tile) out of shared memory.
+  static constexpr uint32_t tmem_cols = 512;
   static constexpr uint32_t col_dq = 256;
-  __device__ static uint32_t ds_addr(uint32_t s0, int t) {
-    return DS_IN_V ? s0 + off_v + (t % NST) * kKV : s0 + off_ds + (t & 1) * kP;
-  }
+  static constexpr uint32_t col_q = 256 + D;
+  static constexpr uint32_t col_do = col_q + D / 2;
+  static constexpr uint32_t col_ds = 16;
 };
+
+// Copies this thread's half row of a 128-byte-swizzled bf16 tile (rows of D
+// values, 64-column chunks 128 * kBM bytes apart) into TMEM lane `lane_addr`
+// as bf16 pairs: D/4 columns starting at column half * D/4.
+template <int D>
+__device__ __forceinline__ void tile_half_row_to_tmem(const uint8_t* tile, int row, int half,
+                                                      uint32_t lane_addr) {
+  constexpr int W = D / 4;  // 32-bit columns per half row
+  uint32_t v[W];
+#pragma unroll
+  for (int q4 = 0; q4 < W / 4; ++q4) {
+    const int byte = half * (D / 2) * 2 + q4 * 16;  // byte offset within the row
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + (byte / 128) * (kBM * 128) +
+                                                    sw128_offset(row, byte % 128));
+    v[4 * q4 + 0] = u.x;
+    v[4 * q4 + 1] = u.y;
+    v[4 * q4 + 2] = u.z;
+    v[4 * q4 + 3] = u.w;
+  }
+#pragma unroll
+  for (int c = 0; c < W; c += 16) SPARGE_TMEM_ST_X16(lane_addr + half * W + c, (v + c));
+}
+
+// tcgen05.mma kind::f16 with the A operand in tensor memory (M lanes, K/2
+// 32-bit columns holding bf16 pairs, element 2c in the low half of column c).
+__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(kGradThreads, 1)
@@ -510,7 +541,7 @@ __global__ void __launch_bounds__(kGradThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == C::B_DSF || i == C::B_DSF + 1) cnt = 32 * kComputeWarps;
+      if (i == C::B_DSF || i == C::B_DSF + 1 || i == C::B_QT) cnt = 32 * kComputeWarps;
       if (i == C::B_DONE) cnt = 2;
       mbar_init(bar(i), cnt);
     }
@@ -544,6 +575,10 @@ __global__ void __launch_bounds__(kGradThreads, 1)
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(s0 + C::off_k + s * C::kKV + c * kBN * 128, &tmK, bar(C::B_KF + s), c * 64,
                       jj * kBN, bh);
+        if (t >= C::NST && !mbar_wait(bar(C::B_VE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+          report_error(status, SPARGE_ERR_TIMEOUT);
+          break;
+        }
         mbar_arrive_expect_tx(bar(C::B_VF + s), C::kKV);
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(s0 + C::off_v + s * C::kKV + c * kBN * 128, &tmV, bar(C::B_VF + s), c * 64,
@@ -556,19 +591,16 @@ __global__ void __launch_bounds__(kGradThreads, 1)
       }
     }
   } else if (warp == kGIssueA) {
-    // S_t = Q K_t^T and dP_t = dO V_t^T.
+    // S_t = Q K_t^T and dP_t = dO V_t^T, with Q and dO read from TMEM.
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-      const uint64_t dq0 = sdesc_sw128(s0 + C::off_q, 16, 1024);
-      const uint64_t ddo0 = sdesc_sw128(s0 + C::off_do, 16, 1024);
-      bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
+      bool ok = mbar_wait(bar(C::B_QT), 0, kWaitTimeoutNs);
       for (int t = 0; ok && t < n; ++t) {
         const int s = t % C::NST;
         const uint32_t dS = tmem + (t & 1) * 128;
-        // TMEM buffer t & 1 was read by the compute warps of tile t - 2 before
-        // they filled dS(t - 2).
+        // TMEM tile t & 1 holds dS(t - 2) until dQ(t - 2) has completed.
         if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs) ||
-            (t >= 2 && !mbar_wait(bar(C::B_DSF + (t & 1)), ((t - 2) >> 1) & 1, kWaitTimeoutNs))) {
+            (t >= 2 && !mbar_wait(bar(C::B_DSE + (t & 1)), ((t - 2) >> 1) & 1, kWaitTimeoutNs))) {
           ok = false;
           break;
         }
@@ -577,9 +609,8 @@ __global__ void __launch_bounds__(kGradThreads, 1)
         const uint64_t dv = sdesc_sw128(s0 + C::off_v + s * C::kKV, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
           const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16(dS, sdesc_add(dq0, ko), sdesc_add(dk, kko), idS, kk > 0);
+          tc_mma_bf16_ta(dS, tmem + C::col_q + kk * 8, sdesc_add(dk, kko), idS, kk > 0);
         }
         if (!mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
           ok = false;
@@ -588,18 +619,18 @@ __global__ void __launch_bounds__(kGradThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
           const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16(dS + 64, sdesc_add(ddo0, ko), sdesc_add(dv, kko), idS, kk > 0);
+          tc_mma_bf16_ta(dS + 64, tmem + C::col_do + kk * 8, sdesc_add(dv, kko), idS, kk > 0);
         }
         tc_commit(bar(C::B_SF + (t & 1)));
+        tc_commit(bar(C::B_VE + s));
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
   } else if (warp == kGIssueB) {
-    // dQ += dS_u K_u (A = dS K-major with K = 64 keys, B = K_u MN-major, N = d).
+    // dQ += dS_u K_u (A = dS_u from TMEM, K = 64 keys; B = K_u MN-major, N = d).
     if (lane == 0 && n > 0) {
       constexpr uint32_t idQ = idesc_bf16(kBM, D, false, true);
       bool ok = true;
@@ -610,14 +641,12 @@ __global__ void __launch_bounds__(kGradThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t dds = sdesc_sw128(C::ds_addr(s0, u), 16, 1024);
+        const uint32_t ads = tmem + (u & 1) * 128 + C::col_ds;
         const uint64_t dk = sdesc_sw128(s0 + C::off_k + su * C::kKV, kBN * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc_mma_bf16(tmem + C::col_dq, sdesc_add(dds, kk * 32), sdesc_add(dk, kk * 2048), idQ,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-        // S/dP(u) completed before dS(u) was written, so stage su is free
-        // once this MMA completes.
+          tc_mma_bf16_ta(tmem + C::col_dq, ads + kk * 8, sdesc_add(dk, kk * 2048), idQ,
+                         (u > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(C::B_KE + su));
         tc_commit(bar(C::B_DSE + (u & 1)));
       }
@@ -635,8 +664,20 @@ __global__ void __launch_bounds__(kGradThreads, 1)
     const float lse2 = (rv && n > 0) ? __ldg(lse + (long long)bh * N + row) * kLog2e : 0.f;
     const float drow = rv ? __ldg(delta + (long long)bh * N + row) : 0.f;
     bool ok = true;
+    // Q and dO into TMEM (this thread's half row of each), for the S and dP
+    // MMAs of every tile.
+    if (n > 0) {
+      ok = warp_wait(bar(C::B_Q), 0);
+      if (ok) {
+        tile_half_row_to_tmem<D>(sm + C::off_q, r, half, lane_base + C::col_q);
+        tile_half_row_to_tmem<D>(sm + C::off_do, r, half, lane_base + C::col_do);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_QT));
+      }
+    }
     int j_next = n > 0 ? min(max(__ldg(list), 0), Mk - 1) : 0;  // one tile ahead
-    for (int t = 0; t < n; ++t) {
+    for (int t = 0; ok && t < n; ++t) {
       const int jj = j_next;
       if (t + 1 < n) j_next = min(max(__ldg(list + t + 1), 0), Mk - 1);
       const int kv_valid = N - jj * kBN;
@@ -659,12 +700,13 @@ __global__ void __launch_bounds__(kGradThreads, 1)
           pk[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
         }
       }
-      if (!C::DS_IN_V && t >= 2 && !warp_wait(bar(C::B_DSE + (t & 1)), ((t - 2) >> 1) & 1)) {
-        ok = false;
-        break;
+      // dS_t over columns col_ds + 16 * half .. + 15 of S_t's tile (this
+      // warp's own S columns, already read into registers above).
+      {
+        const uint32_t da = lane_base + (t & 1) * 128 + C::col_ds + half * 16;
+        SPARGE_TMEM_ST_X16(da, pk);
+        tmem_st_wait();
       }
-      store_half_row_sw128(sm + (C::ds_addr(s0, t) - s0), r, half, pk);
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSF + (t & 1)));
     }
@@ -733,10 +775,8 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   const float scale_log2 = scale * kLog2e;
 
   // Longest lists first: kv-blocks by CSC count, q-blocks by CSR count.
-  order_by_count_kernel<<<1, kOrderThreads, (g.Mq + 1) * sizeof(int32_t), st>>>(
-      col_cnt, g.BH * g.Mk, g.Mq, ws.col_order);
-  order_by_count_kernel<<<1, kOrderThreads, (g.Mk + 1) * sizeof(int32_t), st>>>(
-      row_cnt, g.BH * g.Mq, g.Mk, ws.row_order);
+  order_by_count_kernel<<<1, kOrderThreads, 0, st>>>(col_cnt, g.BH * g.Mk, ws.col_order);
+  order_by_count_kernel<<<1, kOrderThreads, 0, st>>>(row_cnt, g.BH * g.Mq, ws.row_order);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

@@ -42,7 +42,8 @@ cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const v
                             float* lse, int32_t* status, cudaStream_t st);
 
 // attn_bwd.cu.  Workspace: D = rowsum(dO*O) fp32 [BH, N], then the
-// longest-first launch orders of kv-blocks [BH*Mk] and q-blocks [BH*Mq].
+// launch orders of kv-blocks [BH*Mk] and q-blocks [BH*Mq] (long lists first,
+// then index order).
 struct BwdWorkspace {
   float* delta;
   int32_t* col_order;

@@ -176,7 +176,8 @@ int sparge_attn_fwd(const sparge_shape* shape, const void* q, const void* k, con
                     void* o, float* lse, int32_t* status, sparge_stream_t stream);
 
 /* Workspace bytes sparge_attn_bwd needs: fp32 D = rowsum(dO*O) per token and
- * the longest-first launch orders of kv-blocks and q-blocks (int32). */
+ * the launch orders of kv-blocks and q-blocks (int32; lists longer than twice
+ * the mean first, then index order). */
 int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
 
 /*
