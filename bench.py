@@ -13,6 +13,7 @@ Prints one JSON line (rank 0).  ``value`` = kept-FLOP TFLOP/s of fwd+bwd
 the device time of the whole step, mask included.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --sweep     # mask-only and fwd timings over the k x p sweep
 
 Under torchrun (N > 1) every rank runs the same per-GPU workload (heads are
 independent; weak scaling, no data-path collective); the step time is the
@@ -474,6 +475,87 @@ def run_ours(args, wl, k_frac, p):
     return 0
 
 
+# ----------------------------------------------------------------------------- sweep
+SWEEP_K = (0.02, 0.05, 0.10, 0.20)
+SWEEP_P = (0.7, 0.9, 0.97)
+
+
+def run_sweep(args, wl):
+    """Mask-only and forward timings at the 480p shape (N=32760, H=12, d=128)
+    for k in {2, 5, 10, 20}%, p in {0.7, 0.9, 0.97}, on near-uniform pooled
+    rows (Q, K ~ N(0, 0.05^2)) and on sink-dominated rows.  One JSON line."""
+    import ctypes
+    import torch
+    from block_sparse_attention_sparge_gb300 import binding as B
+    from block_sparse_attention_sparge_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B.load_library()
+    Bn, H, N, d = 1, wl.H, wl.N, wl.d
+    mq, mk = -(-N // wl.block_q), -(-N // wl.block_kv)
+    mask_out = B._mask_outputs(Bn, H, mq, mk, dev, False)
+    shp = B.Shape(Bn, H, N, d, wl.block_q, wl.block_kv)
+    nb = ctypes.c_size_t(0)
+    B.load_library().sparge_mask_workspace_bytes(ctypes.byref(shp), ctypes.byref(nb))
+    ws_mask = torch.empty(nb.value, dtype=torch.uint8, device=dev)
+    o = torch.empty((Bn, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Bn, H, N), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(3, min(args.steps, 20))
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    peaks, peak_kind = load_peaks()
+    tc_peak = float(peaks.get("bf16_tflops", peaks.get("bf16_tflops_sustained")))
+    hbm_peak = float(peaks["hbm_gbs"])
+    mask_bytes = 2.0 * Bn * H * N * d * 2
+    cells = []
+    for kind, gen in (("uniform", synth.uniform_inputs), ("skewed", synth.skewed_inputs)):
+        q, k, v, _ = gen(wl, device=dev)
+        for kf in SWEEP_K:
+            for pp in SWEEP_P:
+                res = B.sparge_mask(q, k, kf, pp, out=mask_out, workspace=ws_mask)
+                torch.cuda.synchronize()
+                maskb = unpack_bits(mask_out["bitmask"], mk)
+                pairs = kept_pairs(maskb, N, wl.block_q, wl.block_kv)
+                sparsity = 1.0 - float(maskb.sum().item()) / float(Bn * H * mq * mk)
+                t_mask = timed(lambda: B.sparge_mask(q, k, kf, pp, out=mask_out,
+                                                     workspace=ws_mask))
+                t_fwd = timed(lambda: B.sparge_attn_fwd(q, k, v, res["row_idx"], res["row_cnt"],
+                                                        out=o, lse=lse, status=status))
+                fl = 4.0 * d * pairs
+                cells.append({"rows": kind, "k_frac": kf, "p": pp, "sparsity": round(sparsity, 5),
+                              "mask_ms": round(t_mask, 4),
+                              "mask_frac_hbm": round(mask_bytes / (t_mask * 1e-3) / 1e9 / hbm_peak,
+                                                     3),
+                              "fwd_ms": round(t_fwd, 4),
+                              "fwd_tflops": round(fl / (t_fwd * 1e-3) / 1e12, 1),
+                              "fwd_frac_bf16": round(fl / (t_fwd * 1e-3) / 1e12 / tc_peak, 3)})
+        del q, k, v
+        torch.cuda.empty_cache()
+    if B._read_status(status) != 0:
+        raise RuntimeError("device status set during the sweep")
+    print(json.dumps({
+        "sweep": cells, "reps_per_cell": reps,
+        "workload": (f"{wl.name} shape: B=1, H={H}, N={N}, d={d}, blocks "
+                     f"{wl.block_q}x{wl.block_kv}; uniform rows Q,K~N(0,0.05^2); skewed rows: "
+                     f"kv-block 0 carries K += 2 sqrt(d) u, Q += 0.5 sqrt(d) u"),
+        "mask_ms": "sparge_mask with bitmask and CSR lists (no column lists)",
+        "peaks": f"{peak_kind}: bf16 {tc_peak} TFLOP/s (burst), HBM {hbm_peak} GB/s"}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,6 +569,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="mask-only and fwd timings over k x p on uniform and skewed rows")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -495,6 +579,8 @@ def main(argv=None):
     k_frac = wl.k_frac if args.k_frac is None else args.k_frac
     if args.impl == "reference":
         return run_reference(args, wl, k_frac, args.p)
+    if args.sweep:
+        return run_sweep(args, wl)
     return run_ours(args, wl, k_frac, args.p)
 
 
