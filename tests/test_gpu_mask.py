@@ -162,3 +162,29 @@ def test_mask_is_deterministic():
     for key in ("bitmask", "row_cnt", "col_cnt", "prob"):
         assert torch.equal(a[key], b[key]), key
     assert csr_lists(a["row_idx"], a["row_cnt"]) == csr_lists(b["row_idx"], b["row_cnt"])
+
+
+@pytest.mark.parametrize("mode,settings", [
+    ("topk_only", [(0.01, 0.0), (0.05, 0.0), (0.3, 0.0)]),
+    ("topp_only", [(1e-6, 0.5), (1e-6, 0.9), (1e-6, 0.99)]),
+])
+def test_single_rule_modes(mode, settings):
+    """The two single-rule settings of the one rule: p = 0 gives the Top-k set
+    alone; k_frac <= 1/Mk (K = 1) with p > 0 gives the Top-p set alone (its
+    count is at least 1 whenever p > 0).  Compared with the oracle's
+    single-rule sets row by row."""
+    mk = 200
+    n = mk * 64
+    mq = O.num_blocks(n, 128)
+    rng = np.random.default_rng(17)
+    rows = np.stack([O.row_softmax(rng.normal(scale=s, size=mk)) for s in
+                     np.linspace(0.1, 4.0, mq)]).astype(np.float32)
+    prob = rows[None, None]
+    prob_t = torch.from_numpy(prob).to(DEV)
+    for k_frac, p in settings:
+        res = B.sparge_mask_from_prob(prob_t, k_frac, p, N=n)
+        torch.cuda.synchronize()
+        got = unpack_bitmask(res["bitmask"], mk)[0, 0]
+        for i in range(mq):
+            want = O.topk_set(rows[i], k_frac) if mode == "topk_only" else O.topp_set(rows[i], p)
+            assert set(np.nonzero(got[i])[0].tolist()) == want, (mode, k_frac, p, i)
