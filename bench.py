@@ -42,6 +42,10 @@ METRIC = ("sparse attn fwd+bwd ms & kept-FLOP TFLOP/s at 95% sparsity; "
           "% of BF16/HBM roofline")
 KERNELS_PER_STEP = 9  # pool, select, csc, fwd, delta, 2 x order-by-count, dkdv, dq
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes per call of each entry point (dram__bytes_read.sum + dram__bytes_write.sum
+# summed over its kernels) from one ncu capture of the default workload (480p, k = 5 %,
+# p = 0) with the current kernels; reported as roofline.traffic on that workload only.
+NCU_TRAFFIC_BYTES = {("wan480", 0.05, 0.0): {"bwd": 1527.2e6, "fwd": 344.2e6, "mask": 208.3e6}}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -396,7 +400,8 @@ def run_ours(args, wl, k_frac, p):
                             f" of MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback")
     dom = max(part_ms, key=part_ms.get)
     roofline = dict(roof[dom])
-    roofline["traffic"] = None
+    roofline["traffic"] = NCU_TRAFFIC_BYTES.get((wl.name, k_frac, p), {}).get(dom)
+    roofline["traffic_unit"] = "bytes per call (ncu)"
     roofline["per_launch_ms"] = part_ms[dom]
     roofline["algorithmic"] = {"fwd": "4*d per kept valid (query, key) pair",
                                "bwd": "10*d per kept valid (query, key) pair",
