@@ -611,7 +611,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="wan480", choices=("wan480", "wan720"))
+    ap.add_argument("--workload", default="wan480", choices=("wan480", "wan720", "wan480_d64"))
     ap.add_argument("--k-frac", type=float, default=None)
     ap.add_argument("--p", type=float, default=0.0, help="Top-p of the headline step (0 = off)")
     ap.add_argument("--no-hybrid", action="store_true")

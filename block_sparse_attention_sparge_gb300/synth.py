@@ -68,6 +68,9 @@ WORKLOADS = {
     "tiny": Workload("tiny", 1, 2, (1024,), 64, 128, 64, 0.10, 0.9),
     "wan480": Workload("wan480", 1, 12, (21, 30, 52), 128, 128, 64, 0.05, 0.9),
     "wan720": Workload("wan720", 1, 40, (21, 45, 80), 128, 128, 64, 0.05, 0.9),
+    # The 480p token grid with head width 64 (24 heads: the same model width):
+    # the d = 64 variant of the kernels at full size.
+    "wan480_d64": Workload("wan480_d64", 1, 24, (21, 30, 52), 64, 128, 64, 0.05, 0.9),
 }
 
 # Generator constants (fixed once; recorded in the design notes).
