@@ -10,8 +10,10 @@
 //   dV_j += P^T dO_i,  dK_j += scale * dS^T Q_i,  dQ_i += scale * dS K_j
 // with D_t = sum_c dO_tc O_tc.
 //
-// Three kernels, no atomics (deterministic):
+// Kernels, no atomics (deterministic):
 //   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads).
+//   order_by_count_kernel  launch orders of the two gradient kernels: long
+//                     lists first, then index order (a stable partition).
 //   bwd_dkdv_kernel   one CTA per kv-block, loops over the q-blocks that keep
 //                     it (CSC list).  S and dP are recomputed into TMEM
 //                     (M = 128 query rows); dV^T and dK^T accumulate in TMEM
@@ -23,7 +25,9 @@
 //                     and dS are MMA A operands read from TMEM.
 // Roles per CTA: eight compute warps (two per TMEM lane quarter, each owning
 // 32 of a tile's 64 key columns), a TMA producer warp and two MMA-issuing
-// warps (S and dP; then the gradient MMAs).  Every wait is bounded.
+// warps (S and dP; then the gradient MMAs; two issuers let the gradient MMAs
+// of a tile be queued while the next tile's S and dP are issued).  Every wait
+// is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -19,10 +19,15 @@
 //   T = fl64(p * U), Ti = ceil(T); m_p = smallest m with (sum of the m largest
 //   u in (P desc, index asc) order) >= Ti.  Since partial sums are integers
 //   below 2^53, "fl64(S) >= T" and "S >= ceil(T)" are the same test.
-//   The m_p-th element and the max(K, m_p)-th element are found by a 4-pass
-//   radix select over the 32-bit keys (fp32 bit patterns of P, which order
-//   like the values because P >= 0), with per-warp shared-memory histograms
-//   of counts and u-sums; ties at the threshold key go to the lowest indices.
+//   The keys are the fp32 bit patterns of P, which order like the values
+//   because P >= 0.  One warp selects one row: the Top-p threshold key is the
+//   largest t with (sum of u over keys >= t) >= Ti, and the threshold of the
+//   kept count c = max(K, m_p) the largest t with (count of keys >= t) >= c,
+//   both found by bisection over the 31 key bits with warp reductions (u sums
+//   split into 21-bit halves so the 32-bit reduction is exact); keys equal
+//   to a threshold are kept by lowest index.  Rows longer than 2048 blocks
+//   use a 4-pass radix select with per-warp shared-memory histograms of
+//   counts and u-sums instead.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>

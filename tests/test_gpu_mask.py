@@ -92,7 +92,7 @@ def _adversarial_rows(mk, rng):
     return np.stack(rows).astype(np.float32)
 
 
-@pytest.mark.parametrize("mk", [1, 2, 16, 31, 33, 512, 1182])
+@pytest.mark.parametrize("mk", [1, 2, 16, 31, 33, 512, 1182, 2500])
 def test_select_from_prob_adversarial_rows(mk):
     rng = np.random.default_rng(mk)
     rows = _adversarial_rows(mk, rng)
@@ -188,3 +188,30 @@ def test_single_rule_modes(mode, settings):
         for i in range(mq):
             want = O.topk_set(rows[i], k_frac) if mode == "topk_only" else O.topp_set(rows[i], p)
             assert set(np.nonzero(got[i])[0].tolist()) == want, (mode, k_frac, p, i)
+
+
+@pytest.mark.parametrize("k_frac,p", [(0.05, 0.9), (0.02, 0.0)])
+def test_mask_long_rows(k_frac, p):
+    """Rows of 2500 kv-blocks (N = 160000): above 2048 blocks the selection
+    switches from bisection to the radix select; pooled map within 1e-3 and
+    the mask bit-exact on the GPU's P."""
+    q, k = _rand(1, 1, 160000, 128, seed=41)
+    mq, mk = O.num_blocks(160000, 128), O.num_blocks(160000, 64)
+    res = B.sparge_mask(q.to(DEV), k.to(DEV), k_frac, p, want_prob=True)
+    torch.cuda.synchronize()
+    _, _, _, pr = O.pooled_map(to_np(q), to_np(k), 128, 64)
+    np.testing.assert_allclose(to_np(res["prob"]), pr, atol=MAP_ATOL, rtol=0)
+    _check_mask_against_oracle(res, res["prob"].cpu().numpy(), k_frac, p, mq, mk)
+
+
+def test_mask_custom_scale():
+    """A caller-given softmax scale enters the pooled logits (L = s q̄·k̄)."""
+    q, k = _rand(1, 2, 3000, 64, seed=43)
+    mq, mk = O.num_blocks(3000, 128), O.num_blocks(3000, 64)
+    res = B.sparge_mask(q.to(DEV), k.to(DEV), 0.1, 0.8, softmax_scale=0.3, want_prob=True,
+                        want_logit=True)
+    torch.cuda.synchronize()
+    _, _, lg, pr = O.pooled_map(to_np(q), to_np(k), 128, 64, scale=0.3)
+    np.testing.assert_allclose(to_np(res["logit"]), lg, atol=MAP_ATOL, rtol=0)
+    np.testing.assert_allclose(to_np(res["prob"]), pr, atol=MAP_ATOL, rtol=0)
+    _check_mask_against_oracle(res, res["prob"].cpu().numpy(), 0.1, 0.8, mq, mk)
