@@ -40,12 +40,12 @@ if ROOT not in sys.path:
 
 METRIC = ("sparse attn fwd+bwd ms & kept-FLOP TFLOP/s at 95% sparsity; "
           "% of BF16/HBM roofline")
-KERNELS_PER_STEP = 9  # pool, select, csc, fwd, delta, 2 x order-by-count, dkdv, dq
+KERNELS_PER_STEP = 10  # pool, logits, select, csc, fwd, delta, 2 x order-by-count, dkdv, dq
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes per call of each entry point (dram__bytes_read.sum + dram__bytes_write.sum
 # summed over its kernels) from one ncu capture of the default workload (480p, k = 5 %,
 # p = 0) with the current kernels; reported as roofline.traffic on that workload only.
-NCU_TRAFFIC_BYTES = {("wan480", 0.05, 0.0): {"bwd": 1527.2e6, "fwd": 344.2e6, "mask": 208.3e6}}
+NCU_TRAFFIC_BYTES = {("wan480", 0.05, 0.0): {"bwd": 1527.2e6, "fwd": 344.2e6}}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -390,7 +390,7 @@ def run_ours(args, wl, k_frac, p):
         "bwd": {"kernel": "sparge_attn_bwd (delta + dK/dV + dQ kernels)", "bound": "tensor",
                 "achieved": bwd_flops / (part_ms["bwd"] * 1e-3) / 1e12, "peak": tc_peak,
                 "unit": "TFLOP/s"},
-        "mask": {"kernel": "sparge_mask (pool + score/select + csc kernels)", "bound": "hbm",
+        "mask": {"kernel": "sparge_mask (pool + logits + select + csc kernels)", "bound": "hbm",
                  "achieved": mask_bytes / (part_ms["mask"] * 1e-3) / 1e9, "peak": hbm_peak,
                  "unit": "GB/s"},
     }

@@ -87,11 +87,12 @@ int check_kp(float k_frac, float p) {
   return SPARGE_OK;
 }
 
-// Mask workspace: Q means [BH, Mq, d] and K means transposed [BH, d, Mk],
-// both fp32.
+// Mask workspace: Q means [BH, Mq, d], K means [BH, Mk, d] and the pooled
+// logits [BH, Mq, Mk], all fp32.
 size_t mask_ws_bytes(const Geom& g) {
   return round_up((size_t)g.BH * g.Mq * g.d * sizeof(float)) +
-         round_up((size_t)g.BH * g.d * g.Mk * sizeof(float));
+         round_up((size_t)g.BH * g.Mk * g.d * sizeof(float)) +
+         round_up((size_t)g.BH * g.Mq * g.Mk * sizeof(float));
 }
 
 size_t bwd_ws_bytes(const Geom& g) { return bwd_workspace_bytes(g); }
@@ -169,7 +170,7 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
   SPARGE_TRY(check_tensor(q));
   SPARGE_TRY(check_tensor(k));
   SPARGE_TRY(check_kp(k_frac, p));
-  SPARGE_TRY(check_opt_word(status));  // accepted for symmetry; the mask has no waits
+  SPARGE_TRY(check_opt_word(status));
   if (!isfinite(softmax_scale)) return SPARGE_ERR_INVALID_ARG;
   SPARGE_TRY(check_word(bitmask));
   SPARGE_TRY(check_word(row_idx));
@@ -183,13 +184,17 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
   if (workspace == nullptr || ws_bytes < mask_ws_bytes(g)) return SPARGE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SPARGE_ERR_MISALIGNED;
 
-  float* qbar = static_cast<float*>(workspace);
-  float* kbarT = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                           round_up((size_t)g.BH * g.Mq * g.d * sizeof(float)));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* qbar = reinterpret_cast<float*>(ws);
+  const size_t qbar_bytes = round_up((size_t)g.BH * g.Mq * g.d * sizeof(float));
+  float* kbar = reinterpret_cast<float*>(ws + qbar_bytes);
+  float* logits = reinterpret_cast<float*>(
+      ws + qbar_bytes + round_up((size_t)g.BH * g.Mk * g.d * sizeof(float)));
   const float scale = resolve_scale(softmax_scale, g.d);
-  return cuda_status(launch_mask_pipeline(g, q, k, qbar, kbarT, scale, topk_blocks(k_frac, g.Mk),
-                                          p, bitmask, row_idx, row_cnt, col_idx, col_cnt,
-                                          pooled_logit, pooled_prob, stream));
+  return cuda_status(launch_mask_pipeline(g, q, k, qbar, kbar, logits, scale,
+                                          topk_blocks(k_frac, g.Mk), p, bitmask, row_idx, row_cnt,
+                                          col_idx, col_cnt, pooled_logit, pooled_prob, status,
+                                          stream));
 }
 
 int sparge_mask_from_prob(const sparge_shape* shape, const float* prob, float k_frac, float p,

@@ -28,13 +28,14 @@ cudaError_t launch_select_from_prob(const Geom& g, const float* prob, int ktop, 
                                     cudaStream_t st);
 cudaError_t launch_csc(const Geom& g, const uint32_t* bitmask, int32_t* col_idx, int32_t* col_cnt,
                        cudaStream_t st);
-// The mask as three kernels chained by programmatic dependent launch
-// (mask.cu); kbarT receives the K means transposed, [BH, d, Mk].
+// The mask as kernels chained by programmatic dependent launch (mask.cu):
+// pooling into qbar [BH, Mq, d] and kbar [BH, Mk, d], tensor-core pooled
+// logits into `logits` [BH, Mq, Mk] (fp32), selection, column lists.
 cudaError_t launch_mask_pipeline(const Geom& g, const void* q, const void* k, float* qbar,
-                                 float* kbarT, float scale, int ktop, float p, uint32_t* bitmask,
-                                 int32_t* row_idx, int32_t* row_cnt, int32_t* col_idx,
-                                 int32_t* col_cnt, float* logit_out, float* prob_out,
-                                 cudaStream_t st);
+                                 float* kbar, float* logits, float scale, int ktop, float p,
+                                 uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
+                                 int32_t* col_idx, int32_t* col_cnt, float* logit_out,
+                                 float* prob_out, int32_t* status, cudaStream_t st);
 
 // attn_fwd.cu
 cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const void* v,

@@ -487,29 +487,18 @@ __global__ void __launch_bounds__(kCscThreads) csc_kernel(const uint32_t* __rest
 }
 
 // ---------------------------------------------------------------- mask pipeline
-// sparge_mask runs three kernels chained by programmatic dependent launch:
-//   pool_kernel        Q- and K-block means (HBM-bound, 16-byte loads); for the
-//                      pipeline the K means are stored transposed [BH, d, Mk].
-//   select_kernel      per CTA R q-block rows of one head: pooled logits, row
-//                      softmax, hybrid selection.  Launched while the pooling
-//                      drains; it waits for the pooling's results.
-//   csc_split_kernel   (when the column lists are wanted) per CTA one head and
-//                      32 kv-blocks: the ascending lists of q-blocks, the row
-//                      range split across 8 warps.
+// sparge_mask runs four kernels chained by programmatic dependent launch:
+//   pool_kernel          Q- and K-block means (HBM-bound, 16-byte loads),
+//                        row-major [BH, M, d] fp32.
+//   logits_kernel        L = scale * Qbar Kbar^T per head on the tensor cores,
+//                        one CTA per 128 x 128 tile (below).
+//   select_logits_kernel per CTA up to 8 q-block rows of one head, one warp
+//                        per row: row softmax and hybrid selection.
+//   csc_split_kernel     (when the column lists are wanted) per CTA one head
+//                        and 32 kv-blocks: the ascending lists of q-blocks.
 // A dependent kernel only launches once every CTA of the previous one has
-// started, so its waiting CTAs never keep the previous kernel from running.
-constexpr int kSelkThreads = 256;                   // 8 warps, one row each
-#ifndef SPARGE_SELK_MINB
-#define SPARGE_SELK_MINB 3
-#endif
-constexpr int kSelkRows = kSelkThreads / 32;        // q-blocks per CTA (max)
-constexpr int kSelkLogitFloats = 10240;             // 40 KB of logits per CTA
-
-struct SelkSmem {
-  uint32_t hcnt[kSelkRows][256];                    // radix fallback (Mk > 2048)
-  unsigned long long hsum[kSelkRows][256];
-};
-
+// started and waits for its results itself, so its waiting CTAs never keep
+// the previous kernel from running.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -517,75 +506,189 @@ __device__ __forceinline__ void pdl_wait_primary() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Pooled logits on tcgen05: each fp32 mean x is split into bf16 hi = bf16(x)
+// and lo = bf16(x - hi); per k-step three MMAs accumulate hi.hi + hi.lo +
+// lo.hi in fp32 (the dropped lo.lo term and the rounding of lo are about
+// 2^-16 of each product), so the logits agree with fp32 arithmetic far inside
+// the map tolerance.  Four threads stage each row of the Q tile and of the K
+// tile (a quarter of the row each, all loads in flight at once; 128-byte
+// swizzled, K-major, the layout the MMA descriptors expect), thread 0 issues
+// the MMAs, and warp w reads lanes 32 (w % 4) .. +31, columns 32 (w / 4) .. +31
+// of the accumulator back.
+constexpr int kLgThreads = 512;
+constexpr int kLgTile = 128;
+
 template <int D>
-__global__ void __launch_bounds__(kSelkThreads, SPARGE_SELK_MINB) select_kernel(
-    const float* __restrict__ qbar, const float* __restrict__ kbarT, int Mq, int Mk, int Mkw,
-    int R, float scale, int ktop, float p, uint32_t* __restrict__ bitmask,
-    int32_t* __restrict__ row_idx, int32_t* __restrict__ row_cnt, float* __restrict__ logit_out,
+struct LgCfg {
+  static constexpr uint32_t kTile = kLgTile * D * 2;  // one bf16 [128 x D] tile
+  static constexpr uint32_t off_ahi = 0;
+  static constexpr uint32_t off_alo = kTile;
+  static constexpr uint32_t off_bhi = 2 * kTile;
+  static constexpr uint32_t off_blo = 3 * kTile;
+  static constexpr uint32_t off_bar = 4 * kTile;
+  static constexpr uint32_t smem_alloc = off_bar + 32 + 1024;
+};
+
+// Splits columns [part * D/4, (part + 1) * D/4) of row `src` (D fp32, nullptr
+// = zeros) into bf16 hi / lo, row `row` of two 128-byte-swizzled K-major tiles.
+template <int D>
+__device__ __forceinline__ void stage_split_quarter(const float* src, int row, int part,
+                                                    uint8_t* hi, uint8_t* lo) {
+  constexpr int Q8 = D / 32;  // 8-column groups per quarter row
+  float4 v[2 * Q8];
+#pragma unroll
+  for (int e = 0; e < 2 * Q8; ++e)
+    v[e] = src ? __ldcg(reinterpret_cast<const float4*>(src + part * (D / 4)) + e)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int c8 = 0; c8 < Q8; ++c8) {
+    const float x[8] = {v[2 * c8].x, v[2 * c8].y, v[2 * c8].z, v[2 * c8].w,
+                        v[2 * c8 + 1].x, v[2 * c8 + 1].y, v[2 * c8 + 1].z, v[2 * c8 + 1].w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 hh = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+      const float2 hf = __bfloat1622float2(hh);
+      const __nv_bfloat162 ll = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+      h[e] = *reinterpret_cast<const uint32_t*>(&hh);
+      l[e] = *reinterpret_cast<const uint32_t*>(&ll);
+    }
+    const uint32_t byte = (part * (D / 4) + c8 * 8) * 2;  // within the row of D bf16
+    const uint32_t off = (byte / 128) * (kLgTile * 128) + sw128_offset(row, byte % 128);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kLgThreads, 1) logits_kernel(
+    const float* __restrict__ qbar, const float* __restrict__ kbar, int Mq, int Mk, int nmt,
+    int nnt, float scale, float* __restrict__ logits, int32_t* __restrict__ status) {
+  using C = LgCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t s0 = smem_u32(sm);
+  const uint32_t bar = s0 + C::off_bar;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_bar + 8);
+  const int warp = threadIdx.x >> 5;
+  const int r = threadIdx.x & (kLgTile - 1), part = threadIdx.x / kLgTile;
+  const int per_head = nmt * nnt;
+  const int bh = blockIdx.x / per_head;
+  const int mt = (blockIdx.x % per_head) / nnt;
+  const int nt = blockIdx.x % nnt;
+  const int i = mt * kLgTile + r, j = nt * kLgTile + r;
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(slot), kLgTile);
+    tmem_relinquish();
+  }
+  pdl_wait_primary();  // pooled means are complete and visible
+  stage_split_quarter<D>(i < Mq ? qbar + ((long long)bh * Mq + i) * D : nullptr, r, part,
+                         sm + C::off_ahi, sm + C::off_alo);
+  stage_split_quarter<D>(j < Mk ? kbar + ((long long)bh * Mk + j) * D : nullptr, r, part,
+                         sm + C::off_bhi, sm + C::off_blo);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  if (threadIdx.x == 0) {
+    constexpr uint32_t id = idesc_bf16(kLgTile, kLgTile, false, false);
+    const uint64_t ahi = sdesc_sw128(s0 + C::off_ahi, 16, 1024);
+    const uint64_t alo = sdesc_sw128(s0 + C::off_alo, 16, 1024);
+    const uint64_t bhi = sdesc_sw128(s0 + C::off_bhi, 16, 1024);
+    const uint64_t blo = sdesc_sw128(s0 + C::off_blo, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t ko = (kk >> 2) * (kLgTile * 128) + (kk & 3) * 32;
+      tc_mma_bf16(tmem, sdesc_add(ahi, ko), sdesc_add(bhi, ko), id, kk > 0 ? 1u : 0u);
+      tc_mma_bf16(tmem, sdesc_add(ahi, ko), sdesc_add(blo, ko), id, 1u);
+      tc_mma_bf16(tmem, sdesc_add(alo, ko), sdesc_add(bhi, ko), id, 1u);
+    }
+    tc_commit(bar);
+  }
+  const bool ok = warp_wait(bar, 0);
+  if (!ok && (threadIdx.x & 31) == 0) report_error(status, SPARGE_ERR_TIMEOUT);
+  tc_fence_after();
+  if (ok) {
+    const int quarter = warp & 3, cg = warp >> 2;  // lane quarter, column group
+    const int ri = mt * kLgTile + quarter * 32 + (threadIdx.x & 31);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float* dst = logits + ((long long)bh * Mq + min(ri, Mq - 1)) * Mk + nt * kLgTile;
+    const int ncol = min(kLgTile, Mk - nt * kLgTile);
+    const int i = ri;
+#pragma unroll 1
+    for (int c0 = cg * 32; c0 < cg * 32 + 32; c0 += 16) {
+      uint32_t v[16];
+      SPARGE_TMEM_LD_X16(lane_base + c0, v);
+      SPARGE_TMEM_WAIT_LD16(v);
+      if (i < Mq) {
+        if ((Mk & 3) == 0 && c0 + 16 <= ncol) {  // rows 16-byte aligned
+#pragma unroll
+          for (int c = 0; c < 16; c += 4)
+            *reinterpret_cast<float4*>(dst + c0 + c) =
+                make_float4(__uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
+                            __uint_as_float(v[c + 2]) * scale, __uint_as_float(v[c + 3]) * scale);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (c0 + c < ncol) dst[c0 + c] = __uint_as_float(v[c]) * scale;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kLgTile);
+  }
+}
+
+constexpr int kSelkThreads = 256;                   // 8 warps, one row each
+#ifndef SPARGE_SELK_MINB
+#define SPARGE_SELK_MINB 3
+#endif
+constexpr int kSelkRows = kSelkThreads / 32;        // q-blocks per CTA (max)
+constexpr int kSelkLogitFloats = 10240;             // 40 KB of rows per CTA
+
+struct SelkSmem {
+  uint32_t hcnt[kSelkRows][256];                    // radix fallback (Mk > 2048)
+  unsigned long long hsum[kSelkRows][256];
+};
+
+__global__ void __launch_bounds__(kSelkThreads, SPARGE_SELK_MINB) select_logits_kernel(
+    const float* __restrict__ logits, int Mq, int Mk, int Mkw, int R, int ktop, float p,
+    uint32_t* __restrict__ bitmask, int32_t* __restrict__ row_idx,
+    int32_t* __restrict__ row_cnt, float* __restrict__ logit_out,
     float* __restrict__ prob_out) {
   extern __shared__ __align__(16) uint8_t smem[];
   SelkSmem* hs = reinterpret_cast<SelkSmem*>(smem);
-  float* qs = reinterpret_cast<float*>(smem + sizeof(SelkSmem));  // [D][kSelkRows]
-  float* ls = qs + kSelkRows * D;                                 // [R][Mk]
+  float* ls = reinterpret_cast<float*>(smem + sizeof(SelkSmem));  // [R][Mk]
   const int nrb = (Mq + R - 1) / R;
   const int bh = blockIdx.x / nrb;
   const int i0 = (blockIdx.x % nrb) * R;
   const int nrows = min(R, Mq - i0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  pdl_wait_primary();  // pooled means are complete and visible
+  pdl_wait_primary();  // logits are complete and visible
   pdl_launch_dependents();
-
-  // q rows stored transposed, qs[c * 8 + r], so one pair of 16-byte
-  // broadcast reads gives channel c of all eight rows.
-  const float* qsrc = qbar + ((long long)bh * Mq + i0) * D;
-  for (int t = threadIdx.x; t < kSelkRows * D; t += kSelkThreads) {
-    const int r = t / D, c = t % D;
-    qs[c * kSelkRows + r] = (r < nrows) ? __ldcg(qsrc + t) : 0.f;
-  }
-  __syncthreads();
-
-  // Pooled logits from the transposed K means kbarT[bh][c][j]: a warp reads
-  // 32 consecutive kv-blocks of one channel (one 128-byte line); each thread
-  // carries two columns so that 2 x 16 loads are in flight.  (Wider tiles
-  // per thread leave fewer loads in flight; the phase is bound by L2 latency
-  // and the FMA rate, about 5.6 us of FMA work per SM at the 480p shape.)
-  static_assert(kSelkRows == 8, "two float4 reads cover the q rows");
-  const float* kt = kbarT + (long long)bh * D * Mk;
-  for (int j0 = threadIdx.x; j0 < Mk; j0 += 2 * kSelkThreads) {
-    const int j1 = j0 + kSelkThreads;
-    const bool has1 = j1 < Mk;
-    float a0[kSelkRows], a1[kSelkRows];
-#pragma unroll
-    for (int r = 0; r < kSelkRows; ++r) a0[r] = a1[r] = 0.f;
-#pragma unroll 16
-    for (int c = 0; c < D; ++c) {
-      const float k0 = __ldcg(kt + (long long)c * Mk + j0);
-      const float k1 = has1 ? __ldcg(kt + (long long)c * Mk + j1) : 0.f;
-      const float4 qa = *reinterpret_cast<const float4*>(qs + c * kSelkRows);
-      const float4 qb = *reinterpret_cast<const float4*>(qs + c * kSelkRows + 4);
-      const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-      for (int r = 0; r < kSelkRows; ++r) {
-        a0[r] = fmaf(qv[r], k0, a0[r]);
-        a1[r] = fmaf(qv[r], k1, a1[r]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kSelkRows; ++r) {
-      if (r < nrows) {
-        ls[r * Mk + j0] = a0[r] * scale;
-        if (has1) ls[r * Mk + j1] = a1[r] * scale;
-      }
-    }
-  }
-  __syncthreads();
-
   if (warp < nrows) {
     float* row = ls + warp * Mk;
     const long long grow = (long long)bh * Mq + i0 + warp;
+    const float* src = logits + grow * Mk;
     float m = -INFINITY;
-    for (int j = lane; j < Mk; j += 32) m = fmaxf(m, row[j]);
+    for (int j = lane; j < Mk; j += 32) {
+      const float lg = __ldcg(src + j);
+      row[j] = lg;
+      m = fmaxf(m, lg);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
     float sum = 0.f;
@@ -713,28 +816,37 @@ cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cu
 
 template <int D>
 cudaError_t launch_mask_pipeline_impl(const Geom& g, const void* q, const void* k, float* qbar,
-                                      float* kbarT, float scale, int ktop, float p,
+                                      float* kbar, float* logits, float scale, int ktop, float p,
                                       uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
                                       int32_t* col_idx, int32_t* col_cnt, float* logit_out,
-                                      float* prob_out, cudaStream_t st) {
+                                      float* prob_out, int32_t* status, cudaStream_t st) {
   const long long units = (long long)g.BH * (g.Mq + g.Mk);
   pool_kernel<D><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g.BH, g.N, g.bq,
-      g.bk, g.Mq, g.Mk, 1, qbar, nullptr, kbarT);
+      g.bk, g.Mq, g.Mk, 1, qbar, kbar, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  using L = LgCfg<D>;
+  const int nmt = (g.Mq + kLgTile - 1) / kLgTile, nnt = (g.Mk + kLgTile - 1) / kLgTile;
+  if ((e = cudaFuncSetAttribute(logits_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(L::smem_alloc))) != cudaSuccess)
+    return e;
+  if ((e = launch_pdl(logits_kernel<D>, static_cast<unsigned>((long long)g.BH * nmt * nnt),
+                      kLgThreads, L::smem_alloc, st, static_cast<const float*>(qbar),
+                      static_cast<const float*>(kbar), g.Mq, g.Mk, nmt, nnt, scale, logits,
+                      status)) != cudaSuccess)
+    return e;
   int R = kSelkLogitFloats / g.Mk;
   R = R < 1 ? 1 : (R > kSelkRows ? kSelkRows : R);
   const int nrb = (g.Mq + R - 1) / R;
-  const size_t smem = sizeof(SelkSmem) + (size_t)kSelkRows * D * sizeof(float) +
-                      (size_t)R * g.Mk * sizeof(float);
-  if ((e = cudaFuncSetAttribute(select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = sizeof(SelkSmem) + (size_t)R * g.Mk * sizeof(float);
+  if ((e = cudaFuncSetAttribute(select_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(smem))) != cudaSuccess)
     return e;
-  if ((e = launch_pdl(select_kernel<D>, static_cast<unsigned>((long long)g.BH * nrb),
-                      kSelkThreads, smem, st, static_cast<const float*>(qbar),
-                      static_cast<const float*>(kbarT), g.Mq, g.Mk, g.Mkw, R, scale, ktop, p,
-                      bitmask, row_idx, row_cnt, logit_out, prob_out)) != cudaSuccess)
+  if ((e = launch_pdl(select_logits_kernel, static_cast<unsigned>((long long)g.BH * nrb),
+                      kSelkThreads, smem, st, static_cast<const float*>(logits), g.Mq, g.Mk,
+                      g.Mkw, R, ktop, p, bitmask, row_idx, row_cnt, logit_out, prob_out)) !=
+      cudaSuccess)
     return e;
   if (col_idx != nullptr) {
     e = launch_pdl(csc_split_kernel, static_cast<unsigned>((long long)g.BH * g.Mkw),
@@ -746,15 +858,17 @@ cudaError_t launch_mask_pipeline_impl(const Geom& g, const void* q, const void* 
 }
 
 cudaError_t launch_mask_pipeline(const Geom& g, const void* q, const void* k, float* qbar,
-                                 float* kbarT, float scale, int ktop, float p, uint32_t* bitmask,
-                                 int32_t* row_idx, int32_t* row_cnt, int32_t* col_idx,
-                                 int32_t* col_cnt, float* logit_out, float* prob_out,
-                                 cudaStream_t st) {
+                                 float* kbar, float* logits, float scale, int ktop, float p,
+                                 uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
+                                 int32_t* col_idx, int32_t* col_cnt, float* logit_out,
+                                 float* prob_out, int32_t* status, cudaStream_t st) {
   if (g.d == 128)
-    return launch_mask_pipeline_impl<128>(g, q, k, qbar, kbarT, scale, ktop, p, bitmask, row_idx,
-                                          row_cnt, col_idx, col_cnt, logit_out, prob_out, st);
-  return launch_mask_pipeline_impl<64>(g, q, k, qbar, kbarT, scale, ktop, p, bitmask, row_idx,
-                                       row_cnt, col_idx, col_cnt, logit_out, prob_out, st);
+    return launch_mask_pipeline_impl<128>(g, q, k, qbar, kbar, logits, scale, ktop, p, bitmask,
+                                          row_idx, row_cnt, col_idx, col_cnt, logit_out, prob_out,
+                                          status, st);
+  return launch_mask_pipeline_impl<64>(g, q, k, qbar, kbar, logits, scale, ktop, p, bitmask,
+                                       row_idx, row_cnt, col_idx, col_cnt, logit_out, prob_out,
+                                       status, st);
 }
 
 }  // namespace sparge

@@ -26,9 +26,10 @@
 namespace sparge {
 namespace {
 
-// Upper bound of the scratch: covers B*H*d*(Mq + Mk)*4 bytes up to 8 MiB, e.g.
-// the 480p video shape (B=1, H=12, N=32760, d=128) needs 4.7 MB.
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+// Upper bound of the scratch: pooled Q and K (B*H*d*(Mq + Mk)*4 bytes) and
+// the pooled logits (B*H*Mq*Mk*4 bytes) up to 16 MiB, e.g. the 480p video
+// shape (B=1, H=12, N=32760, d=128) needs 10.9 MB.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_mask_scratch[kNoAllocScratchBytes];
 

@@ -105,12 +105,13 @@ int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes);
  *   pooled_logit : fp32 [B,H,Mq,Mk] out, L (nullable).
  *   pooled_prob  : fp32 [B,H,Mq,Mk] out, P (nullable).
  *   workspace    : device buffer of sparge_mask_workspace_bytes bytes (pooled
- *                  Q and K; no initial contents needed).
+ *                  Q and K, pooled logits; no initial contents needed).
  *   status       : nullable; unused (the mask kernels have no internal waits).
  * The mask is a deterministic function of the fp32 P it computes.  The call
- * launches three kernels (two without the column lists) chained by
- * programmatic dependent launch: pooling, then pooled map and selection,
- * then the column lists.
+ * launches four kernels (three without the column lists) chained by
+ * programmatic dependent launch: pooling, pooled logits on the tensor cores
+ * (fp32 means split into bf16 high and low parts, three MMA passes),
+ * softmax and selection, then the column lists.
  */
 int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k_frac, float p,
                 float softmax_scale, uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
@@ -124,9 +125,9 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
  * allocation or free may synchronise the device).  The method pages have no
  * counterpart of this call; it is a deployment variant of sparge_mask.
  *   Same arguments, outputs and results as sparge_mask, minus workspace and
- *   ws_bytes.  The pooled Q and K live in a fixed 8 MiB device array inside
+ *   ws_bytes.  The pooled Q, K and logits live in a fixed 16 MiB device array inside
  *   the library, one per GPU that loads it, kept until the process exits.
- *   Shapes whose workspace (sparge_mask_workspace_bytes) exceeds 8 MiB return
+ *   Shapes whose workspace (sparge_mask_workspace_bytes) exceeds 16 MiB return
  *   SPARGE_ERR_WORKSPACE before any launch.
  *   The first call on a device (made with that device current) looks up the
  *   array's device address once; make that first call before any stream
