@@ -87,11 +87,11 @@ int check_kp(float k_frac, float p) {
   return SPARGE_OK;
 }
 
-// Mask workspace: Q means [BH, Mq, d], K means [BH, Mk, d] and the pooled
-// logits [BH, Mq, Mk], all fp32.
+// Mask workspace: the Q means [BH, Mq, d] and the K means [BH, Mk, d], each
+// as a bf16 pair hi, lo (four arrays), then the pooled logits [BH, Mq, Mk]
+// fp32.
 size_t mask_ws_bytes(const Geom& g) {
-  return round_up((size_t)g.BH * g.Mq * g.d * sizeof(float)) +
-         round_up((size_t)g.BH * g.Mk * g.d * sizeof(float)) +
+  return 2 * round_up((size_t)g.BH * g.Mq * g.d * 2) + 2 * round_up((size_t)g.BH * g.Mk * g.d * 2) +
          round_up((size_t)g.BH * g.Mq * g.Mk * sizeof(float));
 }
 
@@ -185,13 +185,15 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SPARGE_ERR_MISALIGNED;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* qbar = reinterpret_cast<float*>(ws);
-  const size_t qbar_bytes = round_up((size_t)g.BH * g.Mq * g.d * sizeof(float));
-  float* kbar = reinterpret_cast<float*>(ws + qbar_bytes);
-  float* logits = reinterpret_cast<float*>(
-      ws + qbar_bytes + round_up((size_t)g.BH * g.Mk * g.d * sizeof(float)));
+  const size_t qb = round_up((size_t)g.BH * g.Mq * g.d * 2);
+  const size_t kb = round_up((size_t)g.BH * g.Mk * g.d * 2);
+  void* qhi = ws;
+  void* qlo = ws + qb;
+  void* khi = ws + 2 * qb;
+  void* klo = ws + 2 * qb + kb;
+  float* logits = reinterpret_cast<float*>(ws + 2 * qb + 2 * kb);
   const float scale = resolve_scale(softmax_scale, g.d);
-  return cuda_status(launch_mask_pipeline(g, q, k, qbar, kbar, logits, scale,
+  return cuda_status(launch_mask_pipeline(g, q, k, qhi, qlo, khi, klo, logits, scale,
                                           topk_blocks(k_frac, g.Mk), p, bitmask, row_idx, row_cnt,
                                           col_idx, col_cnt, pooled_logit, pooled_prob, status,
                                           stream));

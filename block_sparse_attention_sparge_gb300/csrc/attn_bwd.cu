@@ -142,20 +142,6 @@ __device__ __forceinline__ void store_half_row_sw128(uint8_t* tile, int row, int
   }
 }
 
-// Loads 32 fp32 columns of one TMEM lane starting at `addr`.
-__device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&x)[32]) {
-  uint32_t ra[16], rb[16];
-  SPARGE_TMEM_LD_X16(addr + 0, ra);
-  SPARGE_TMEM_LD_X16(addr + 16, rb);
-  SPARGE_TMEM_WAIT_LD16(ra);
-  SPARGE_TMEM_WAIT_LD16(rb);
-#pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    x[c] = __uint_as_float(ra[c]);
-    x[16 + c] = __uint_as_float(rb[c]);
-  }
-}
-
 // Warp roles of both gradient kernels (352 threads): warps 0-7 compute, with
 // query row (or feature) 32*(w % 4) + lane = TMEM lane and score columns
 // 32*(w / 4) .. +31 (P comes from the saved LSE, so a row needs no exchange
@@ -428,9 +414,9 @@ __global__ void __launch_bounds__(kGradThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           if (cc + c < kv_valid) {
-            dv[base + (long long)(cc + c) * D] = __float2bfloat16_rn(__uint_as_float(rv_[c]));
-            dk[base + (long long)(cc + c) * D] =
-                __float2bfloat16_rn(__uint_as_float(rk_[c]) * scale);
+            __stcs(dv + base + (long long)(cc + c) * D, __float2bfloat16_rn(__uint_as_float(rv_[c])));
+            __stcs(dk + base + (long long)(cc + c) * D,
+                   __float2bfloat16_rn(__uint_as_float(rk_[c]) * scale));
           }
         }
       }
@@ -742,8 +728,8 @@ __global__ void __launch_bounds__(kGradThreads, 1)
       w1.z = pack_bf16x2(__uint_as_float(ro[12]) * scale, __uint_as_float(ro[13]) * scale);
       w1.w = pack_bf16x2(__uint_as_float(ro[14]) * scale, __uint_as_float(ro[15]) * scale);
       if (rv) {
-        *reinterpret_cast<uint4*>(qrow + cc) = w0;
-        *reinterpret_cast<uint4*>(qrow + cc + 8) = w1;
+        __stcs(reinterpret_cast<uint4*>(qrow + cc), w0);
+        __stcs(reinterpret_cast<uint4*>(qrow + cc + 8), w1);
       }
     }
   }

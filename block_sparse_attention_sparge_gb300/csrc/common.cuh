@@ -209,6 +209,21 @@ SPARGE_DEV uint32_t sw128_offset(uint32_t row, uint32_t col_bytes) {
                  "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),  \
                  "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory")
 
+// Loads 32 fp32 columns of one TMEM lane starting at `addr` (warp-wide;
+// the warp's lane quarter is the one it may access).
+SPARGE_DEV void tmem_ld32(uint32_t addr, float (&x)[32]) {
+  uint32_t ra[16], rb[16];
+  SPARGE_TMEM_LD_X16(addr + 0, ra);
+  SPARGE_TMEM_LD_X16(addr + 16, rb);
+  SPARGE_TMEM_WAIT_LD16(ra);
+  SPARGE_TMEM_WAIT_LD16(rb);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    x[c] = __uint_as_float(ra[c]);
+    x[16 + c] = __uint_as_float(rb[c]);
+  }
+}
+
 #define SPARGE_TMEM_ST_X16(taddr, r)                                                        \
   asm volatile(                                                                             \
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \

@@ -31,11 +31,12 @@ cudaError_t launch_csc(const Geom& g, const uint32_t* bitmask, int32_t* col_idx,
 // The mask as kernels chained by programmatic dependent launch (mask.cu):
 // pooling into qbar [BH, Mq, d] and kbar [BH, Mk, d], tensor-core pooled
 // logits into `logits` [BH, Mq, Mk] (fp32), selection, column lists.
-cudaError_t launch_mask_pipeline(const Geom& g, const void* q, const void* k, float* qbar,
-                                 float* kbar, float* logits, float scale, int ktop, float p,
-                                 uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
-                                 int32_t* col_idx, int32_t* col_cnt, float* logit_out,
-                                 float* prob_out, int32_t* status, cudaStream_t st);
+cudaError_t launch_mask_pipeline(const Geom& g, const void* q, const void* k, void* qhi,
+                                 void* qlo, void* khi, void* klo, float* logits, float scale,
+                                 int ktop, float p, uint32_t* bitmask, int32_t* row_idx,
+                                 int32_t* row_cnt, int32_t* col_idx, int32_t* col_cnt,
+                                 float* logit_out, float* prob_out, int32_t* status,
+                                 cudaStream_t st);
 
 // attn_fwd.cu
 cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const void* v,

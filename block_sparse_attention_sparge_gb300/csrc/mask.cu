@@ -8,9 +8,10 @@
 // Kernel-Implementierung und Modellanpassung" (mask construction in CUDA).
 //
 // Kernels:
-//   pool_kernel, select_kernel, csc_split_kernel  the sparge_mask pipeline
-//                        (see "mask pipeline" below); pool_kernel alone also
-//                        serves sparge_pool.
+//   pool_kernel, logits_kernel, select_logits_reg_kernel (rows up to 512
+//                        blocks) or select_logits_kernel, csc_split_kernel
+//                        the sparge_mask pipeline (see "mask pipeline"
+//                        below); pool_kernel alone also serves sparge_pool.
 //   select_from_prob_kernel  the selection alone on a given probability map.
 //   csc_kernel           transposes the bitmask into per-kv-block q lists.
 //
@@ -23,11 +24,13 @@
 //   because P >= 0.  One warp selects one row: the Top-p threshold key is the
 //   largest t with (sum of u over keys >= t) >= Ti, and the threshold of the
 //   kept count c = max(K, m_p) the largest t with (count of keys >= t) >= c,
-//   both found by bisection over the 31 key bits with warp reductions (u sums
-//   split into 21-bit halves so the 32-bit reduction is exact); keys equal
-//   to a threshold are kept by lowest index.  Rows longer than 2048 blocks
+//   both found by bisection over the key bits with warp reductions (u sums
+//   split into 21-bit halves so the 32-bit reduction is exact), starting
+//   below the bits that every key of the row shares; keys equal to a
+//   threshold are kept by lowest index.  Rows longer than 2048 blocks
 //   use a 4-pass radix select with per-warp shared-memory histograms of
 //   counts and u-sums instead.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -42,21 +45,21 @@ namespace sparge {
 
 namespace {
 
-constexpr int kPoolThreads = 256;
 constexpr int kSelThreads = 512;               // 16 warps, one row each
 constexpr int kSelMaxRows = kSelThreads / 32;  // rows per CTA upper bound
 constexpr int kSelLogitFloats = 20480;         // 80 KB of logits per CTA
 constexpr unsigned kFull = 0xffffffffu;
 
 // ---------------------------------------------------------------- pooling
-// Mean of `rows` rows of one block (d = D bf16 values per row), written to
-// out[t * stride] for channel t.  Thread i reads 16-byte chunk (i % CH) of
-// rows i / CH, + RG, ...; the partial sums meet in `red`.  The caller
+constexpr int kPoolThreads = 256;
+
+// Mean of `rows` rows of one block (d = D bf16 values per row); thread
+// t < D returns channel t.  Thread i reads 16-byte chunk (i % CH) of rows
+// i / CH, + RG, ...; the partial sums meet in `red`.  The caller
 // synchronises before reusing `red`.
 template <int D>
-__device__ __forceinline__ void pool_block(const __nv_bfloat16* __restrict__ src, int rows,
-                                           float (*red)[D], float* __restrict__ out,
-                                           long long stride) {
+__device__ __forceinline__ float pool_block(const __nv_bfloat16* __restrict__ src, int rows,
+                                            float (*red)[D]) {
   constexpr int CH = D / 8;              // 16-byte chunks per row
   constexpr int RG = kPoolThreads / CH;  // rows read concurrently
   const int c = threadIdx.x % CH;
@@ -80,22 +83,25 @@ __device__ __forceinline__ void pool_block(const __nv_bfloat16* __restrict__ src
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[rg][c * 8 + e] = acc[e];
   __syncthreads();
+  float s = 0.f;
   if (threadIdx.x < D) {
-    float s = 0.f;
 #pragma unroll
     for (int g = 0; g < RG; ++g) s += red[g][threadIdx.x];
-    out[threadIdx.x * stride] = s / static_cast<float>(rows);
   }
+  return s / static_cast<float>(rows);
 }
 
-// One CTA per (head, block) unit.  Units [0, BH*Mq) are Q blocks, the rest K
-// blocks.  Q means are row-major [BH, Mq, d]; K means row-major [BH, Mk, d]
-// into kbar, or transposed [BH, d, Mk] into kbarT when that is set.
+// One CTA per (head, block) unit.  Units [0, BH*Mq) are Q blocks (when
+// do_q), the rest K blocks.  The means are row-major [BH, M, d]: fp32 into
+// qbar / kbar, or, when qhi is set, as the bf16 pair hi = bf16(mean),
+// lo = bf16(mean - hi) into qhi / qlo and khi / klo (the operands of the
+// pooled-logit MMAs, hi*hi + hi*lo + lo*hi).
 template <int D>
 __global__ void __launch_bounds__(kPoolThreads) pool_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int BH, int N,
     int bq, int bk, int Mq, int Mk, int do_q, float* __restrict__ qbar,
-    float* __restrict__ kbar, float* __restrict__ kbarT) {
+    float* __restrict__ kbar, __nv_bfloat16* __restrict__ qhi, __nv_bfloat16* __restrict__ qlo,
+    __nv_bfloat16* __restrict__ khi, __nv_bfloat16* __restrict__ klo) {
   // Lets a kernel launched with programmatic serialization start early; it
   // waits for this grid's results itself.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -111,12 +117,31 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(
   const int r0 = i * blk;
   const __nv_bfloat16* src = (is_q ? q : k) + ((long long)bh * N + r0) * D;
   const int rows = min(blk, N - r0);
-  if (is_q)
-    pool_block<D>(src, rows, red, qbar + ((long long)bh * Mq + i) * D, 1);
-  else if (kbarT)
-    pool_block<D>(src, rows, red, kbarT + (long long)bh * D * Mk + i, Mk);
-  else
-    pool_block<D>(src, rows, red, kbar + ((long long)bh * Mk + i) * D, 1);
+  const float mean = pool_block<D>(src, rows, red);
+  if (threadIdx.x < D) {
+    const long long o = ((long long)bh * M + i) * D + threadIdx.x;
+    if (qhi != nullptr) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(mean);
+      const __nv_bfloat16 l = __float2bfloat16_rn(mean - __bfloat162float(h));
+      (is_q ? qhi : khi)[o] = h;
+      (is_q ? qlo : klo)[o] = l;
+    } else {
+      (is_q ? qbar : kbar)[o] = mean;
+    }
+  }
+}
+
+// One CTA per unit (units = the Q and K blocks to pool).
+template <int D>
+cudaError_t launch_pool_kernel(const Geom& g, const void* q, const void* k, int do_q,
+                               long long units, float* qbar, float* kbar, void* qhi, void* qlo,
+                               void* khi, void* klo, cudaStream_t st) {
+  pool_kernel<D><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g.BH, g.N, g.bq,
+      g.bk, g.Mq, g.Mk, do_q, qbar, kbar, static_cast<__nv_bfloat16*>(qhi),
+      static_cast<__nv_bfloat16*>(qlo), static_cast<__nv_bfloat16*>(khi),
+      static_cast<__nv_bfloat16*>(klo));
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- selection
@@ -290,43 +315,63 @@ __device__ __forceinline__ unsigned long long warp_sum_u42(unsigned long long v)
   return (static_cast<unsigned long long>(a) << 42) + (static_cast<unsigned long long>(b) << 21) + c;
 }
 
-// Hybrid Top-k + Top-p selection of one row (one warp), keys in registers.
-// Lane l holds elements j = 32 e + l (e < EPL).  The thresholds are found by
-// a bitwise binary search on the fp32 key: the largest key tau with
+// Hybrid Top-k + Top-p selection of one row (one warp).  Lane l holds
+// elements j = 32 e + l (e < EPL): with kRegs their fp32 keys come in kr[],
+// else they are read from `keys` in shared memory.  The thresholds are found
+// by a bitwise binary search on the fp32 key: the largest key tau with
 // sum_{key >= tau} u >= Ti (Top-p) or #{key >= tau} >= c (Top-k/union);
 // absent elements carry key 0, which no candidate (>= 1) admits.  Results
 // equal select_row's exactly (same integer rule, same tie order).
 template <int EPL, bool kRegs>
-__device__ void select_row_reg(const float* prow, int Mk, int ktop, float p,
-                               uint32_t* __restrict__ bm_row, int32_t* __restrict__ idx_row,
-                               int32_t* __restrict__ cnt_out) {
+__device__ __forceinline__ void select_keys(const uint32_t (&kr)[kRegs ? EPL : 1],
+                                            const uint32_t* keys, int Mk, int ktop, float p,
+                                            uint32_t* __restrict__ bm_row,
+                                            int32_t* __restrict__ idx_row,
+                                            int32_t* __restrict__ cnt_out) {
   const int lane = threadIdx.x & 31;
-  const uint32_t* keys = reinterpret_cast<const uint32_t*>(prow);
   // Elements per lane actually present (EPL is the compile-time bound).  The
-  // loops below unroll fully over EPL so that kr[] stays in registers; in
-  // shared-memory mode they stop at ne.
+  // loops below unroll fully over EPL so that register arrays stay in
+  // registers; in shared-memory mode they stop at ne.
   const int ne = kRegs ? EPL : (Mk + 31) / 32;
-  uint32_t kr[kRegs ? EPL : 1];
-  if (kRegs) {
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const int j = e * 32 + lane;
-      kr[kRegs ? e : 0] = j < Mk ? keys[j] : 0u;
-    }
-  }
   // Element e of this lane (absent elements read as key 0).
   auto key_of = [&](int e) -> uint32_t {
     if (kRegs) return kr[kRegs ? e : 0];
     const int j = e * 32 + lane;
     return j < Mk ? keys[j] : 0u;
   };
-  auto u_of = [&](int, uint32_t k) -> unsigned long long { return fixed40(k); };
+  // Bits above `hb` are the same in every present key (`base` holds them):
+  // a search candidate that differs from base there admits all keys or none,
+  // so both searches below start at bit hb from base (hb = -1: all keys
+  // equal, base is the key).
+  uint32_t kor = 0u, kand = ~0u;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    if (!kRegs && e >= ne) break;
+    const uint32_t k = key_of(e);
+    kor |= k;
+    kand &= (e * 32 + lane < Mk) ? k : ~0u;
+  }
+  kor = __reduce_or_sync(kFull, kor);
+  kand = __reduce_and_sync(kFull, kand);
+  const uint32_t diff = kor ^ kand;
+  const int hb = diff ? 31 - __clz(static_cast<int>(diff)) : -1;
+  const uint32_t base = hb >= 0 ? (kand & ~((2u << hb) - 1u)) : kand;
   int m_p;
   if (p >= 1.f) {
     m_p = Mk;
   } else if (!(p > 0.f)) {
     m_p = 0;
   } else {
+    // u = floor(P * 2^40) of each element, computed once when the keys are
+    // in registers.
+    unsigned long long ur[kRegs ? EPL : 1];
+    if (kRegs) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) ur[kRegs ? e : 0] = fixed40(key_of(e));
+    }
+    auto u_of = [&](int e, uint32_t k) -> unsigned long long {
+      return kRegs ? ur[kRegs ? e : 0] : fixed40(k);
+    };
     unsigned long long part = 0;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
@@ -339,8 +384,9 @@ __device__ void select_row_reg(const float* prow, int Mk, int ktop, float p,
     if (Ti == 0ull) {
       m_p = 0;
     } else {
-      uint32_t tau = 0;
-      for (int bit = 30; bit >= 0; --bit) {
+      // sum_{key >= base} u = U >= Ti, so base qualifies.
+      uint32_t tau = base;
+      for (int bit = hb; bit >= 0; --bit) {
         const uint32_t cand = tau | (1u << bit);
         unsigned long long s = 0;
 #pragma unroll
@@ -371,9 +417,12 @@ __device__ void select_row_reg(const float* prow, int Mk, int ktop, float p,
   const int c = min(Mk, max(ktop, m_p));
   // tau_c: a key with exactly c keys >= it if one exists (the search stops
   // there), else the c-th largest key; either way the kept set below is the
-  // c keys >= tau_c, ties at tau_c taken by lower index.
-  uint32_t tau_c = 0;
-  for (int bit = 30; bit >= 0; --bit) {
+  // c keys >= tau_c, ties at tau_c taken by lower index.  All Mk keys are
+  // >= base, so base qualifies for c >= 1 (c = 0 keeps nothing: tau_c stays
+  // above every key).
+  uint32_t tau_c = c > 0 ? base : 0x7fffffffu;
+  bool exact = (c == Mk);  // exactly c keys >= tau_c
+  for (int bit = hb; c > 0 && !exact && bit >= 0; --bit) {
     const uint32_t cand = tau_c | (1u << bit);
     uint32_t n = 0;
 #pragma unroll
@@ -384,18 +433,22 @@ __device__ void select_row_reg(const float* prow, int Mk, int ktop, float p,
     const int tot = static_cast<int>(__reduce_add_sync(kFull, n));
     if (tot >= c) {
       tau_c = cand;
-      if (tot == c) break;
+      exact = (tot == c);
     }
   }
-  uint32_t ngt = 0;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    if (!kRegs && e >= ne) break;
-    ngt += key_of(e) > tau_c ? 1u : 0u;
-  }
   // Keys equal to tau_c are real elements or, when tau_c is 0, zero
-  // probabilities; absent elements are excluded below by j < Mk.
-  const int need_ties = c - static_cast<int>(__reduce_add_sync(kFull, ngt));
+  // probabilities; absent elements are excluded below by j < Mk.  When
+  // exactly c keys are >= tau_c, every tie is kept.
+  int need_ties = 0;
+  if (!exact) {
+    uint32_t ngt = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      if (!kRegs && e >= ne) break;
+      ngt += key_of(e) > tau_c ? 1u : 0u;
+    }
+    need_ties = c - static_cast<int>(__reduce_add_sync(kFull, ngt));
+  }
   const uint32_t lt = (1u << lane) - 1u;
   int ties = 0, kept = 0;
 #pragma unroll
@@ -404,12 +457,17 @@ __device__ void select_row_reg(const float* prow, int Mk, int ktop, float p,
     const int j = e * 32 + lane;
     const bool valid = j < Mk;
     const uint32_t k = key_of(e);
-    const bool gt = valid && k > tau_c;
-    const bool eq = valid && k == tau_c;
-    const uint32_t em = __ballot_sync(kFull, eq);
-    const int rank = ties + __popc(em & lt);
-    const bool keep = gt || (eq && rank < need_ties);
-    ties += __popc(em);
+    bool keep;
+    if (exact) {
+      keep = valid && k >= tau_c;
+    } else {
+      const bool gt = valid && k > tau_c;
+      const bool eq = valid && k == tau_c;
+      const uint32_t em = __ballot_sync(kFull, eq);
+      const int rank = ties + __popc(em & lt);
+      keep = gt || (eq && rank < need_ties);
+      ties += __popc(em);
+    }
     const uint32_t km = __ballot_sync(kFull, keep);
     if (e * 32 < Mk) {
       if (lane == 0) bm_row[e] = km;
@@ -418,6 +476,27 @@ __device__ void select_row_reg(const float* prow, int Mk, int ktop, float p,
     kept += __popc(km);
   }
   if (lane == 0) *cnt_out = kept;
+}
+
+// select_keys on a row of probabilities in shared memory: copied into
+// registers first (kRegs) or read in place.
+template <int EPL, bool kRegs>
+__device__ void select_row_reg(const float* prow, int Mk, int ktop, float p,
+                               uint32_t* __restrict__ bm_row, int32_t* __restrict__ idx_row,
+                               int32_t* __restrict__ cnt_out) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t* keys = reinterpret_cast<const uint32_t*>(prow);
+  uint32_t kr[kRegs ? EPL : 1];
+  if (kRegs) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const int j = e * 32 + lane;
+      kr[kRegs ? e : 0] = j < Mk ? keys[j] : 0u;
+    }
+  } else {
+    kr[0] = 0u;
+  }
+  select_keys<EPL, kRegs>(kr, keys, Mk, ktop, p, bm_row, idx_row, cnt_out);
 }
 
 // Binary search with keys in registers for rows up to 512 blocks, reading
@@ -489,11 +568,13 @@ __global__ void __launch_bounds__(kCscThreads) csc_kernel(const uint32_t* __rest
 // ---------------------------------------------------------------- mask pipeline
 // sparge_mask runs four kernels chained by programmatic dependent launch:
 //   pool_kernel          Q- and K-block means (HBM-bound, 16-byte loads),
-//                        row-major [BH, M, d] fp32.
+//                        row-major [BH, M, d] as bf16 hi / lo pairs.
 //   logits_kernel        L = scale * Qbar Kbar^T per head on the tensor cores,
 //                        one CTA per 128 x 128 tile (below).
-//   select_logits_kernel per CTA up to 8 q-block rows of one head, one warp
-//                        per row: row softmax and hybrid selection.
+//   select_logits_reg_kernel  one warp per q-block row, the row's logits in
+//                        registers (Mk <= 512): row softmax and hybrid
+//                        selection; select_logits_kernel stages longer rows
+//                        in shared memory.
 //   csc_split_kernel     (when the column lists are wanted) per CTA one head
 //                        and 32 kv-blocks: the ascending lists of q-blocks.
 // A dependent kernel only launches once every CTA of the previous one has
@@ -506,123 +587,104 @@ __device__ __forceinline__ void pdl_wait_primary() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// Pooled logits on tcgen05: each fp32 mean x is split into bf16 hi = bf16(x)
-// and lo = bf16(x - hi); per k-step three MMAs accumulate hi.hi + hi.lo +
-// lo.hi in fp32 (the dropped lo.lo term and the rounding of lo are about
-// 2^-16 of each product), so the logits agree with fp32 arithmetic far inside
-// the map tolerance.  Four threads stage each row of the Q tile and of the K
-// tile (a quarter of the row each, all loads in flight at once; 128-byte
-// swizzled, K-major, the layout the MMA descriptors expect), thread 0 issues
-// the MMAs, and warp w reads lanes 32 (w % 4) .. +31, columns 32 (w / 4) .. +31
-// of the accumulator back.
+// Pooled logits on tcgen05: each fp32 mean x is held as bf16 hi = bf16(x)
+// and lo = bf16(x - hi) (written so by the pooling kernel); per k-step three
+// MMAs accumulate hi.hi + hi.lo + lo.hi in fp32 (the dropped lo.lo term and
+// the rounding of lo are about 2^-16 of each product), so the logits agree
+// with fp32 arithmetic far inside the map tolerance.  Thread 0 loads the four
+// tiles by TMA (128-byte swizzled, K-major, the layout the MMA descriptors
+// expect) and issues the MMAs, and warp w reads lanes 32 (w % 4) .. +31,
+// columns 32 (w / 4) .. +31 of the accumulator back.
 constexpr int kLgThreads = 512;
 constexpr int kLgTile = 128;
 
 template <int D>
 struct LgCfg {
+  static constexpr int KCH = D / 64;                  // 128-byte column chunks per row
   static constexpr uint32_t kTile = kLgTile * D * 2;  // one bf16 [128 x D] tile
   static constexpr uint32_t off_ahi = 0;
   static constexpr uint32_t off_alo = kTile;
   static constexpr uint32_t off_bhi = 2 * kTile;
   static constexpr uint32_t off_blo = 3 * kTile;
-  static constexpr uint32_t off_bar = 4 * kTile;
-  static constexpr uint32_t smem_alloc = off_bar + 32 + 1024;
+  static constexpr uint32_t off_bar = 4 * kTile;      // [0] operands landed, [1] MMAs done
+  static constexpr uint32_t off_slot = off_bar + 16;
+  static constexpr uint32_t smem_alloc = off_slot + 16 + 1024;
 };
 
-// Splits columns [part * D/4, (part + 1) * D/4) of row `src` (D fp32, nullptr
-// = zeros) into bf16 hi / lo, row `row` of two 128-byte-swizzled K-major tiles.
-template <int D>
-__device__ __forceinline__ void stage_split_quarter(const float* src, int row, int part,
-                                                    uint8_t* hi, uint8_t* lo) {
-  constexpr int Q8 = D / 32;  // 8-column groups per quarter row
-  float4 v[2 * Q8];
-#pragma unroll
-  for (int e = 0; e < 2 * Q8; ++e)
-    v[e] = src ? __ldcg(reinterpret_cast<const float4*>(src + part * (D / 4)) + e)
-               : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int c8 = 0; c8 < Q8; ++c8) {
-    const float x[8] = {v[2 * c8].x, v[2 * c8].y, v[2 * c8].z, v[2 * c8].w,
-                        v[2 * c8 + 1].x, v[2 * c8 + 1].y, v[2 * c8 + 1].z, v[2 * c8 + 1].w};
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat162 hh = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-      const float2 hf = __bfloat1622float2(hh);
-      const __nv_bfloat162 ll = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
-      h[e] = *reinterpret_cast<const uint32_t*>(&hh);
-      l[e] = *reinterpret_cast<const uint32_t*>(&ll);
-    }
-    const uint32_t byte = (part * (D / 4) + c8 * 8) * 2;  // within the row of D bf16
-    const uint32_t off = (byte / 128) * (kLgTile * 128) + sw128_offset(row, byte % 128);
-    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
+// Pooled logits of one 128 x 128 tile (q-blocks mt*128.., k-blocks nt*128..)
+// of head bh: scale * (Qhi Khi^T + Qhi Klo^T + Qlo Khi^T) on the tensor
+// cores, the split-bf16 means loaded by TMA (rows past Mq / Mk read as zero).
 template <int D>
 __global__ void __launch_bounds__(kLgThreads, 1) logits_kernel(
-    const float* __restrict__ qbar, const float* __restrict__ kbar, int Mq, int Mk, int nmt,
-    int nnt, float scale, float* __restrict__ logits, int32_t* __restrict__ status) {
+    const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmQl,
+    const __grid_constant__ CUtensorMap tmKh, const __grid_constant__ CUtensorMap tmKl, int Mq,
+    int Mk, int nmt, int nnt, float scale, float* __restrict__ logits,
+    int32_t* __restrict__ status) {
   using C = LgCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const uint32_t s0 = smem_u32(sm);
-  const uint32_t bar = s0 + C::off_bar;
-  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_bar + 8);
+  const uint32_t bar_ld = s0 + C::off_bar, bar_mma = s0 + C::off_bar + 8;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
   const int warp = threadIdx.x >> 5;
-  const int r = threadIdx.x & (kLgTile - 1), part = threadIdx.x / kLgTile;
   const int per_head = nmt * nnt;
   const int bh = blockIdx.x / per_head;
   const int mt = (blockIdx.x % per_head) / nnt;
   const int nt = blockIdx.x % nnt;
-  const int i = mt * kLgTile + r, j = nt * kLgTile + r;
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+    mbar_init(bar_ld, 1);
+    mbar_init(bar_mma, 1);
     fence_barrier_init();
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(slot), kLgTile);
     tmem_relinquish();
   }
-  pdl_wait_primary();  // pooled means are complete and visible
-  stage_split_quarter<D>(i < Mq ? qbar + ((long long)bh * Mq + i) * D : nullptr, r, part,
-                         sm + C::off_ahi, sm + C::off_alo);
-  stage_split_quarter<D>(j < Mk ? kbar + ((long long)bh * Mk + j) * D : nullptr, r, part,
-                         sm + C::off_bhi, sm + C::off_blo);
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
   if (threadIdx.x == 0) {
-    constexpr uint32_t id = idesc_bf16(kLgTile, kLgTile, false, false);
-    const uint64_t ahi = sdesc_sw128(s0 + C::off_ahi, 16, 1024);
-    const uint64_t alo = sdesc_sw128(s0 + C::off_alo, 16, 1024);
-    const uint64_t bhi = sdesc_sw128(s0 + C::off_bhi, 16, 1024);
-    const uint64_t blo = sdesc_sw128(s0 + C::off_blo, 16, 1024);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t ko = (kk >> 2) * (kLgTile * 128) + (kk & 3) * 32;
-      tc_mma_bf16(tmem, sdesc_add(ahi, ko), sdesc_add(bhi, ko), id, kk > 0 ? 1u : 0u);
-      tc_mma_bf16(tmem, sdesc_add(ahi, ko), sdesc_add(blo, ko), id, 1u);
-      tc_mma_bf16(tmem, sdesc_add(alo, ko), sdesc_add(bhi, ko), id, 1u);
+    pdl_wait_primary();  // the pooled means are complete and visible
+    mbar_arrive_expect_tx(bar_ld, 4 * C::kTile);
+    for (int c = 0; c < C::KCH; ++c) {
+      const uint32_t co = c * (kLgTile * 128);
+      tma_load_3d(s0 + C::off_ahi + co, &tmQh, bar_ld, c * 64, mt * kLgTile, bh);
+      tma_load_3d(s0 + C::off_alo + co, &tmQl, bar_ld, c * 64, mt * kLgTile, bh);
+      tma_load_3d(s0 + C::off_bhi + co, &tmKh, bar_ld, c * 64, nt * kLgTile, bh);
+      tma_load_3d(s0 + C::off_blo + co, &tmKl, bar_ld, c * 64, nt * kLgTile, bh);
     }
-    tc_commit(bar);
+    if (mbar_wait(bar_ld, 0, kWaitTimeoutNs)) {
+      tc_fence_after();
+      constexpr uint32_t id = idesc_bf16(kLgTile, kLgTile, false, false);
+      const uint64_t ahi = sdesc_sw128(s0 + C::off_ahi, 16, 1024);
+      const uint64_t alo = sdesc_sw128(s0 + C::off_alo, 16, 1024);
+      const uint64_t bhi = sdesc_sw128(s0 + C::off_bhi, 16, 1024);
+      const uint64_t blo = sdesc_sw128(s0 + C::off_blo, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * (kLgTile * 128) + (kk & 3) * 32;
+        tc_mma_bf16(tmem, sdesc_add(ahi, ko), sdesc_add(bhi, ko), id, kk > 0 ? 1u : 0u);
+        tc_mma_bf16(tmem, sdesc_add(ahi, ko), sdesc_add(blo, ko), id, 1u);
+        tc_mma_bf16(tmem, sdesc_add(alo, ko), sdesc_add(bhi, ko), id, 1u);
+      }
+    } else {
+      report_error(status, SPARGE_ERR_TIMEOUT);
+    }
+    tc_commit(bar_mma);
   }
-  const bool ok = warp_wait(bar, 0);
+  const bool ok = warp_wait(bar_mma, 0);
   if (!ok && (threadIdx.x & 31) == 0) report_error(status, SPARGE_ERR_TIMEOUT);
   tc_fence_after();
   if (ok) {
     const int quarter = warp & 3, cg = warp >> 2;  // lane quarter, column group
-    const int ri = mt * kLgTile + quarter * 32 + (threadIdx.x & 31);
+    const int i = mt * kLgTile + quarter * 32 + (threadIdx.x & 31);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* dst = logits + ((long long)bh * Mq + min(ri, Mq - 1)) * Mk + nt * kLgTile;
+    float* dst = logits + ((long long)bh * Mq + min(i, Mq - 1)) * Mk + nt * kLgTile;
     const int ncol = min(kLgTile, Mk - nt * kLgTile);
-    const int i = ri;
 #pragma unroll 1
     for (int c0 = cg * 32; c0 < cg * 32 + 32; c0 += 16) {
       uint32_t v[16];
@@ -649,6 +711,59 @@ __global__ void __launch_bounds__(kLgThreads, 1) logits_kernel(
     tc_fence_after();
     tmem_dealloc(tmem, kLgTile);
   }
+}
+
+// Row softmax and hybrid selection with the row in registers (Mk <= 32*EPL):
+// one warp per q-block row, all of the row's loads in flight at once.
+constexpr int kSelrThreads = 256;
+template <int EPL>
+__global__ void __launch_bounds__(kSelrThreads) select_logits_reg_kernel(
+    const float* __restrict__ logits, int rows, int Mk, int Mkw, int ktop, float p,
+    uint32_t* __restrict__ bitmask, int32_t* __restrict__ row_idx,
+    int32_t* __restrict__ row_cnt, float* __restrict__ logit_out,
+    float* __restrict__ prob_out) {
+  const int lane = threadIdx.x & 31;
+  const long long grow = (long long)blockIdx.x * (kSelrThreads / 32) + (threadIdx.x >> 5);
+  pdl_wait_primary();  // logits are complete and visible
+  pdl_launch_dependents();
+  if (grow >= rows) return;
+  const float* src = logits + grow * Mk;
+  float x[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const int j = e * 32 + lane;
+    x[e] = j < Mk ? __ldcg(src + j) : -INFINITY;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) m = fmaxf(m, x[e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  // exp(x - m) = 2^(x log2 e - m log2 e); P = e * (1 / sum), within 2 ulp of
+  // the correctly rounded quotient.
+  constexpr float kL2e = 1.4426950408889634f;
+  const float ml = m * kL2e;
+  float sum = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const int j = e * 32 + lane;
+    if (logit_out && j < Mk) logit_out[grow * Mk + j] = x[e];
+    x[e] = j < Mk ? ex2_approx(fmaf(x[e], kL2e, -ml)) : 0.f;
+    sum += x[e];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+  const float inv = __frcp_rn(sum);
+  uint32_t kr[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const int j = e * 32 + lane;
+    const float pj = x[e] * inv;
+    kr[e] = __float_as_uint(pj);  // absent elements: 0 / sum = +0, key 0
+    if (prob_out && j < Mk) prob_out[grow * Mk + j] = pj;
+  }
+  select_keys<EPL, true>(kr, nullptr, Mk, ktop, p, bitmask + grow * Mkw, row_idx + grow * Mk,
+                         row_cnt + grow);
 }
 
 constexpr int kSelkThreads = 256;                   // 8 warps, one row each
@@ -712,43 +827,59 @@ __global__ void __launch_bounds__(kSelkThreads, SPARGE_SELK_MINB) select_logits_
   }
 }
 
-// CTA = (head, bitmask word w), 8 warps.  Warp g scans rows [g*Mq/8, (g+1)*Mq/8)
-// of kv-blocks 32w + lane, counts them, and after a prefix over the warps
-// writes its q-block indices at their ascending positions.
+// CTA = (head, bitmask word w), 8 warps; the columns are the 32 kv-blocks
+// 32w + b.  Rows go in passes of 256, thread t holding the word of row
+// pass*256 + t.  Per column b, warp g's 32 rows form the ballot of bit b:
+// its popcount is the warp's count, and after an exclusive scan over the
+// warps (plus the counts of earlier passes) each set lane writes its row at
+// offset + rank, so the column's rows land contiguously in ascending order.
 constexpr int kCscSplitThreads = 256;
 __global__ void __launch_bounds__(kCscSplitThreads) csc_split_kernel(
     const uint32_t* __restrict__ bitmask, int Mq, int Mk, int Mkw, int32_t* __restrict__ col_idx,
     int32_t* __restrict__ col_cnt) {
-  extern __shared__ uint32_t words[];  // [Mq]
-  __shared__ int cnt_w[8][32];
+  constexpr int W = kCscSplitThreads / 32;
+  __shared__ int cnt_w[W][32];
+  __shared__ int run[32];
   pdl_wait_primary();
   const int bh = blockIdx.x / Mkw;
   const int w = blockIdx.x % Mkw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1u;
   const uint32_t* src = bitmask + (long long)bh * Mq * Mkw + w;
-  for (int i = threadIdx.x; i < Mq; i += kCscSplitThreads)
-    words[i] = __ldcg(src + (long long)i * Mkw);
-  __syncthreads();
-  const int per = (Mq + 7) / 8;
-  const int lo = min(Mq, warp * per), hi = min(Mq, lo + per);
-  int cnt = 0;
-  for (int i = lo; i < hi; ++i) cnt += (words[i] >> lane) & 1u;
-  cnt_w[warp][lane] = cnt;
-  __syncthreads();
-  int off = 0, total = 0;
+  const int ncol = min(32, Mk - w * 32);
+  int32_t* out0 = col_idx + ((long long)bh * Mk + w * 32) * Mq;
+  if (threadIdx.x < 32) run[threadIdx.x] = 0;
+  for (int r0 = 0; r0 < Mq; r0 += kCscSplitThreads) {
+    const int i = r0 + threadIdx.x;
+    const uint32_t word = i < Mq ? __ldcg(src + (long long)i * Mkw) : 0u;
+    // Lane b keeps this warp's count of column b.
+    int mine = 0;
+#pragma unroll 8
+    for (int b = 0; b < 32; ++b) {
+      const int n = __popc(__ballot_sync(kFull, (word >> b) & 1u));
+      if (lane == b) mine = n;
+    }
+    cnt_w[warp][lane] = mine;
+    __syncthreads();
+    int off = run[lane];
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const int c = cnt_w[g][lane];
-    off += g < warp ? c : 0;
-    total += c;
+    for (int g = 0; g < W; ++g) off += g < warp ? cnt_w[g][lane] : 0;
+#pragma unroll 4
+    for (int b = 0; b < ncol; ++b) {
+      const uint32_t m = __ballot_sync(kFull, (word >> b) & 1u);
+      const int ob = __shfl_sync(kFull, off, b);
+      if ((word >> b) & 1u) out0[(long long)b * Mq + ob + __popc(m & lt)] = i;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      int t = 0;
+#pragma unroll
+      for (int g = 0; g < W; ++g) t += cnt_w[g][threadIdx.x];
+      run[threadIdx.x] += t;
+    }
+    __syncthreads();
   }
-  const int j = w * 32 + lane;
-  if (j < Mk) {
-    int32_t* out = col_idx + ((long long)bh * Mk + j) * Mq + off;
-    for (int i = lo; i < hi; ++i)
-      if ((words[i] >> lane) & 1u) *out++ = i;
-    if (warp == 0) col_cnt[(long long)bh * Mk + j] = total;
-  }
+  if (threadIdx.x < ncol) col_cnt[(long long)bh * Mk + w * 32 + threadIdx.x] = run[threadIdx.x];
 }
 
 }  // namespace
@@ -764,15 +895,11 @@ cudaError_t launch_pool(const Geom& g, const void* q, const void* k, float* qbar
   const int do_k = kbar != nullptr;
   const long long units = (do_q ? (long long)g.BH * g.Mq : 0) + (do_k ? (long long)g.BH * g.Mk : 0);
   if (units == 0) return cudaSuccess;
-  const auto* qq = static_cast<const __nv_bfloat16*>(q);
-  const auto* kk = static_cast<const __nv_bfloat16*>(k);
   if (g.d == 128)
-    pool_kernel<128><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
-        qq, kk, g.BH, g.N, g.bq, g.bk, g.Mq, g.Mk, do_q, qbar, kbar, nullptr);
-  else
-    pool_kernel<64><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
-        qq, kk, g.BH, g.N, g.bq, g.bk, g.Mq, g.Mk, do_q, qbar, kbar, nullptr);
-  return cudaGetLastError();
+    return launch_pool_kernel<128>(g, q, k, do_q, units, qbar, kbar, nullptr, nullptr, nullptr,
+                                   nullptr, st);
+  return launch_pool_kernel<64>(g, q, k, do_q, units, qbar, kbar, nullptr, nullptr, nullptr,
+                                nullptr, st);
 }
 
 cudaError_t launch_select_from_prob(const Geom& g, const float* prob, int ktop, float p,
@@ -815,16 +942,20 @@ cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cu
 }
 
 template <int D>
-cudaError_t launch_mask_pipeline_impl(const Geom& g, const void* q, const void* k, float* qbar,
-                                      float* kbar, float* logits, float scale, int ktop, float p,
-                                      uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
-                                      int32_t* col_idx, int32_t* col_cnt, float* logit_out,
-                                      float* prob_out, int32_t* status, cudaStream_t st) {
-  const long long units = (long long)g.BH * (g.Mq + g.Mk);
-  pool_kernel<D><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g.BH, g.N, g.bq,
-      g.bk, g.Mq, g.Mk, 1, qbar, kbar, nullptr);
-  cudaError_t e = cudaGetLastError();
+cudaError_t launch_mask_pipeline_impl(const Geom& g, const void* q, const void* k, void* qhi,
+                                      void* qlo, void* khi, void* klo, float* logits, float scale,
+                                      int ktop, float p, uint32_t* bitmask, int32_t* row_idx,
+                                      int32_t* row_cnt, int32_t* col_idx, int32_t* col_cnt,
+                                      float* logit_out, float* prob_out, int32_t* status,
+                                      cudaStream_t st) {
+  CUtensorMap tqh, tql, tkh, tkl;
+  if (make_tmap_bf16(&tqh, qhi, g.BH, g.Mq, D, kLgTile) != 0 ||
+      make_tmap_bf16(&tql, qlo, g.BH, g.Mq, D, kLgTile) != 0 ||
+      make_tmap_bf16(&tkh, khi, g.BH, g.Mk, D, kLgTile) != 0 ||
+      make_tmap_bf16(&tkl, klo, g.BH, g.Mk, D, kLgTile) != 0)
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_pool_kernel<D>(g, q, k, 1, (long long)g.BH * (g.Mq + g.Mk), nullptr,
+                                        nullptr, qhi, qlo, khi, klo, st);
   if (e != cudaSuccess) return e;
   using L = LgCfg<D>;
   const int nmt = (g.Mq + kLgTile - 1) / kLgTile, nnt = (g.Mk + kLgTile - 1) / kLgTile;
@@ -832,42 +963,55 @@ cudaError_t launch_mask_pipeline_impl(const Geom& g, const void* q, const void* 
                                 static_cast<int>(L::smem_alloc))) != cudaSuccess)
     return e;
   if ((e = launch_pdl(logits_kernel<D>, static_cast<unsigned>((long long)g.BH * nmt * nnt),
-                      kLgThreads, L::smem_alloc, st, static_cast<const float*>(qbar),
-                      static_cast<const float*>(kbar), g.Mq, g.Mk, nmt, nnt, scale, logits,
-                      status)) != cudaSuccess)
+                      kLgThreads, L::smem_alloc, st, tqh, tql, tkh, tkl, g.Mq, g.Mk, nmt, nnt,
+                      scale, logits, status)) != cudaSuccess)
     return e;
-  int R = kSelkLogitFloats / g.Mk;
-  R = R < 1 ? 1 : (R > kSelkRows ? kSelkRows : R);
-  const int nrb = (g.Mq + R - 1) / R;
-  const size_t smem = sizeof(SelkSmem) + (size_t)R * g.Mk * sizeof(float);
-  if ((e = cudaFuncSetAttribute(select_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem))) != cudaSuccess)
-    return e;
-  if ((e = launch_pdl(select_logits_kernel, static_cast<unsigned>((long long)g.BH * nrb),
-                      kSelkThreads, smem, st, static_cast<const float*>(logits), g.Mq, g.Mk,
-                      g.Mkw, R, ktop, p, bitmask, row_idx, row_cnt, logit_out, prob_out)) !=
-      cudaSuccess)
-    return e;
+  if (g.Mk <= 32 * 16) {
+    const long long rows = (long long)g.BH * g.Mq;
+    constexpr int kRowsPerCta = kSelrThreads / 32;
+    if ((e = launch_pdl(select_logits_reg_kernel<16>,
+                        static_cast<unsigned>((rows + kRowsPerCta - 1) / kRowsPerCta),
+                        kSelrThreads, 0, st, static_cast<const float*>(logits),
+                        static_cast<int>(rows), g.Mk, g.Mkw, ktop, p, bitmask, row_idx, row_cnt,
+                        logit_out, prob_out)) != cudaSuccess)
+      return e;
+  } else {
+    int R = kSelkLogitFloats / g.Mk;
+    R = R < 1 ? 1 : (R > kSelkRows ? kSelkRows : R);
+    const int nrb = (g.Mq + R - 1) / R;
+    const size_t smem = sizeof(SelkSmem) + (size_t)R * g.Mk * sizeof(float);
+    if ((e = cudaFuncSetAttribute(select_logits_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(smem))) != cudaSuccess)
+      return e;
+    if ((e = launch_pdl(select_logits_kernel, static_cast<unsigned>((long long)g.BH * nrb),
+                        kSelkThreads, smem, st, static_cast<const float*>(logits), g.Mq, g.Mk,
+                        g.Mkw, R, ktop, p, bitmask, row_idx, row_cnt, logit_out, prob_out)) !=
+        cudaSuccess)
+      return e;
+  }
   if (col_idx != nullptr) {
     e = launch_pdl(csc_split_kernel, static_cast<unsigned>((long long)g.BH * g.Mkw),
-                   kCscSplitThreads, (size_t)g.Mq * sizeof(uint32_t), st,
+                   kCscSplitThreads, 0, st,
                    static_cast<const uint32_t*>(bitmask), g.Mq, g.Mk, g.Mkw, col_idx, col_cnt);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_mask_pipeline(const Geom& g, const void* q, const void* k, float* qbar,
-                                 float* kbar, float* logits, float scale, int ktop, float p,
-                                 uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
-                                 int32_t* col_idx, int32_t* col_cnt, float* logit_out,
-                                 float* prob_out, int32_t* status, cudaStream_t st) {
+cudaError_t launch_mask_pipeline(const Geom& g, const void* q, const void* k, void* qhi,
+                                 void* qlo, void* khi, void* klo, float* logits, float scale,
+                                 int ktop, float p, uint32_t* bitmask, int32_t* row_idx,
+                                 int32_t* row_cnt, int32_t* col_idx, int32_t* col_cnt,
+                                 float* logit_out, float* prob_out, int32_t* status,
+                                 cudaStream_t st) {
   if (g.d == 128)
-    return launch_mask_pipeline_impl<128>(g, q, k, qbar, kbar, logits, scale, ktop, p, bitmask,
-                                          row_idx, row_cnt, col_idx, col_cnt, logit_out, prob_out,
-                                          status, st);
-  return launch_mask_pipeline_impl<64>(g, q, k, qbar, kbar, logits, scale, ktop, p, bitmask,
-                                       row_idx, row_cnt, col_idx, col_cnt, logit_out, prob_out,
+    return launch_mask_pipeline_impl<128>(g, q, k, qhi, qlo, khi, klo, logits, scale, ktop, p,
+                                          bitmask, row_idx, row_cnt, col_idx, col_cnt, logit_out,
+                                          prob_out, status, st);
+  return launch_mask_pipeline_impl<64>(g, q, k, qhi, qlo, khi, klo, logits, scale, ktop, p,
+                                       bitmask, row_idx, row_cnt, col_idx, col_cnt, logit_out,
+                                       prob_out,
                                        status, st);
 }
 

@@ -75,7 +75,8 @@ const char* sparge_status_string(int status);
 int sparge_pool(const sparge_shape* shape, const void* q, const void* k, float* qbar,
                 float* kbar, sparge_stream_t stream);
 
-/* Workspace bytes sparge_mask needs (pooled Q and K, fp32). */
+/* Workspace bytes sparge_mask needs (pooled Q and K as bf16 high / low
+ * pairs, the fp32 pooled logits). */
 int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes);
 
 /*
@@ -105,13 +106,16 @@ int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes);
  *   pooled_logit : fp32 [B,H,Mq,Mk] out, L (nullable).
  *   pooled_prob  : fp32 [B,H,Mq,Mk] out, P (nullable).
  *   workspace    : device buffer of sparge_mask_workspace_bytes bytes (pooled
- *                  Q and K, pooled logits; no initial contents needed).
- *   status       : nullable; unused (the mask kernels have no internal waits).
+ *                  Q and K, pooled logits; no initial contents needed),
+ *                  16-byte aligned.
+ *   status       : nullable; records SPARGE_ERR_TIMEOUT if a bounded wait of
+ *                  the pooled-logit kernel runs out.
  * The mask is a deterministic function of the fp32 P it computes.  The call
  * launches four kernels (three without the column lists) chained by
- * programmatic dependent launch: pooling, pooled logits on the tensor cores
- * (fp32 means split into bf16 high and low parts, three MMA passes),
- * softmax and selection, then the column lists.
+ * programmatic dependent launch: pooling (each mean written as bf16 high
+ * and low parts), pooled logits on the tensor cores (three MMA passes over
+ * the parts, operands loaded by TMA), softmax and selection, then the
+ * column lists.
  */
 int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k_frac, float p,
                 float softmax_scale, uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,

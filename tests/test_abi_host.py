@@ -59,9 +59,10 @@ def test_workspace_sizes(lib):
     s = _shape(1, 12, 32760, 128)
     assert lib.sparge_mask_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 0
     mq, mk = 256, 512
-    # Q means, K means and the pooled logits, fp32, each region 256-byte aligned.
-    expect = 12 * mq * 128 * 4 + 12 * mk * 128 * 4 + 12 * mq * mk * 4
-    assert expect <= n.value <= expect + 3 * 256
+    # Q and K means as bf16 pairs (hi, lo) and the fp32 pooled logits, each of
+    # the five regions 256-byte aligned.
+    expect = 2 * 12 * mq * 128 * 2 + 2 * 12 * mk * 128 * 2 + 12 * mq * mk * 4
+    assert expect <= n.value <= expect + 5 * 256
     assert lib.sparge_attn_bwd_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 0
     expect = 12 * 32760 * 4 + 12 * 512 * 4 + 12 * 256 * 4
     assert expect <= n.value <= expect + 3 * 256
