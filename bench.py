@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per call of each entry point (dram__bytes_read.sum + dram__bytes_write.sum
 # summed over its kernels) from one ncu capture of the default workload (480p, k = 5 %,
 # p = 0) with the current kernels; reported as roofline.traffic on that workload only.
-NCU_TRAFFIC_BYTES = {("wan480", 0.05, 0.0): {"bwd": 1529.2e6, "fwd": 344.5e6}}
+NCU_TRAFFIC_BYTES = {("wan480", 0.05, 0.0): {"bwd": 1522.9e6, "fwd": 343.9e6, "mask": 214.4e6}}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -407,6 +407,28 @@ def run_ours(args, wl, k_frac, p):
                                "bwd": "10*d per kept valid (query, key) pair",
                                "mask": "Q+K read once + bitmask, CSR/CSC and counts written"}[dom]
 
+    # The mask alone: 50 calls back to back (Q + K = 201 MB at 480p, above the
+    # L2 size), with and without the column lists the backward uses; the
+    # bitmask + CSR output is the mask construction proper.
+    mask_alone = None
+    if not args.no_hybrid:
+        mo_csr = B._mask_outputs(Bn, H, mq, mk, dev, False)
+        alone = {}
+        for name, mo in (("with_csc", mask_out), ("csr_only", mo_csr)):
+            for _ in range(3):
+                B.sparge_mask(q, k, k_frac, p, out=mo, workspace=ws_mask)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(50):
+                B.sparge_mask(q, k, k_frac, p, out=mo, workspace=ws_mask)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / 50
+            nbytes = mask_bytes if name == "with_csc" else mask_bytes - kept_tiles * 4 - Bn * H * mk * 4
+            alone[name] = {"ms": ms, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9,
+                           "frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak}
+        mask_alone = {"calls": 50, "note": "sparge_mask timed alone, calls back to back", **alone}
+
     # hybrid rule (the workload's p) on the same inputs
     hybrid = None
     if not args.no_hybrid:
@@ -509,6 +531,7 @@ def run_ours(args, wl, k_frac, p):
             "dense_equiv_tflops": 14.0 * d * float(Bn * H) * N * N * ws / (ms_step * 1e-3) / 1e12,
             "roofline": roofline,
             "roofline_all": roof,
+            "mask_alone": mask_alone,
             "hybrid": hybrid,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
