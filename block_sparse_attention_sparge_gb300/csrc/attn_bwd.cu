@@ -12,8 +12,9 @@
 //
 // Kernels, no atomics (deterministic):
 //   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads).
-//   order_by_count_kernel  launch orders of the two gradient kernels: long
-//                     lists first, then index order (a stable partition).
+//   (two extra CTAs of the delta grid) launch orders of the two gradient
+//                     kernels: long lists first, then index order (a stable
+//                     partition).
 //   bwd_dkdv_kernel   one CTA per kv-block, loops over the q-blocks that keep
 //                     it (CSC list).  S and dP are recomputed into TMEM
 //                     (M = 128 query rows); dV^T and dK^T accumulate in TMEM
@@ -45,11 +46,78 @@ constexpr int kBM = 128;
 constexpr int kBN = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// ---------------------------------------------------------------- work order
+// Launch order of the gradient CTAs: the lists longer than twice the mean
+// first, then the others, each group in index order (a stable partition).
+// Long lists (attention-sink blocks that nearly every q-block keeps) would
+// otherwise run alone at the end of the grid; index order keeps the CTAs of
+// one head together, so that head's Q/dO (or K/V) tiles are served from L2.
+// One CTA of NT threads partitions the n items.
+template <int NT>
+__device__ void order_by_count(const int32_t* __restrict__ cnt, int n, int32_t* __restrict__ order) {
+  constexpr int W = NT / 32;
+  __shared__ long long red[W];
+  __shared__ int scan[W];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int E = (n + NT - 1) / NT;
+  const int lo = min(n, tid * E), hi = min(n, lo + E);
+  // Total of the counts.
+  long long sum = 0;
+  for (int it = lo; it < hi; ++it) sum += max(__ldg(cnt + it), 0);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) red[w] = sum;
+  __syncthreads();
+  long long total = 0;
+#pragma unroll
+  for (int i = 0; i < W; ++i) total += red[i];
+  // Item `it` is long when cnt * n > 2 * total.
+  auto is_long = [&](int it) { return (long long)max(__ldg(cnt + it), 0) * n > 2 * total; };
+  int nl = 0;
+  for (int it = lo; it < hi; ++it) nl += is_long(it) ? 1 : 0;
+  // Exclusive scan of the per-thread long counts.
+  int incl = nl;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) scan[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < W ? scan[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += v;
+    }
+    if (lane < W) scan[lane] = t;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int before_long = incl - nl + (w > 0 ? scan[w - 1] : 0);
+  const int n_long = scan[W - 1];
+  int pl = before_long;                // next long position
+  int ps = n_long + lo - before_long;  // next short position
+  for (int it = lo; it < hi; ++it) order[is_long(it) ? pl++ : ps++] = it;
+}
+
 // ---------------------------------------------------------------- D = rowsum(dO * O)
+// CTAs [0, ndelta) compute D; the two CTAs after them build the launch orders
+// of the kv-blocks and of the q-blocks while the rest of the grid streams O
+// and dO.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                                        const __nv_bfloat16* __restrict__ dout,
-                                                        long long rows, float* __restrict__ delta) {
+__global__ void __launch_bounds__(256) bwd_delta_kernel(
+    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, long long rows,
+    float* __restrict__ delta, unsigned ndelta, const int32_t* __restrict__ col_cnt, int ncol,
+    int32_t* __restrict__ col_order, const int32_t* __restrict__ row_cnt, int nrow,
+    int32_t* __restrict__ row_order) {
+  if (blockIdx.x >= ndelta) {
+    if (blockIdx.x == ndelta)
+      order_by_count<256>(col_cnt, ncol, col_order);
+    else
+      order_by_count<256>(row_cnt, nrow, row_order);
+    return;
+  }
   constexpr int CH = D / 8;        // 16-byte chunks per row
   constexpr int RPB = 256 / CH;    // rows per block pass
   const long long r = (long long)blockIdx.x * RPB + threadIdx.x / CH;
@@ -71,60 +139,6 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 #pragma unroll
   for (int off = CH / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (c == 0 && r < rows) delta[r] = s;
-}
-
-// ---------------------------------------------------------------- work order
-// Launch order of the gradient CTAs: the lists longer than twice the mean
-// first, then the others, each group in index order (a stable partition).
-// Long lists (attention-sink blocks that nearly every q-block keeps) would
-// otherwise run alone at the end of the grid; index order keeps the CTAs of
-// one head together, so that head's Q/dO (or K/V) tiles are served from L2.
-constexpr int kOrderThreads = 1024;
-__global__ void __launch_bounds__(kOrderThreads) order_by_count_kernel(
-    const int32_t* __restrict__ cnt, int n, int32_t* __restrict__ order) {
-  __shared__ long long red[kOrderThreads / 32];
-  __shared__ int scan[kOrderThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int E = (n + kOrderThreads - 1) / kOrderThreads;
-  const int lo = min(n, tid * E), hi = min(n, lo + E);
-  // Total of the counts.
-  long long sum = 0;
-  for (int it = lo; it < hi; ++it) sum += max(__ldg(cnt + it), 0);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) red[w] = sum;
-  __syncthreads();
-  long long total = 0;
-#pragma unroll 4
-  for (int i = 0; i < kOrderThreads / 32; ++i) total += red[i];
-  // Item `it` is long when cnt * n > 2 * total.
-  auto is_long = [&](int it) { return (long long)max(__ldg(cnt + it), 0) * n > 2 * total; };
-  int nl = 0;
-  for (int it = lo; it < hi; ++it) nl += is_long(it) ? 1 : 0;
-  // Exclusive scan of the per-thread long counts.
-  int incl = nl;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) scan[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int t = scan[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += v;
-    }
-    scan[lane] = t;  // inclusive warp totals
-  }
-  __syncthreads();
-  const int before_long = incl - nl + (w > 0 ? scan[w - 1] : 0);
-  const int n_long = scan[kOrderThreads / 32 - 1];
-  int pl = before_long;            // next long position
-  int ps = n_long + lo - before_long;  // next short position
-  for (int it = lo; it < hi; ++it) order[is_long(it) ? pl++ : ps++] = it;
 }
 
 // Writes 32 bf16 values (half of a 128-byte row: 16-byte chunks 4h .. 4h+3)
@@ -195,6 +209,9 @@ __global__ void __launch_bounds__(kGradThreads, 1)
                     float scale_log2, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, int32_t* __restrict__ status) {
   using C = DkdvCfg<D>;
+  // The dQ kernel (independent of this one) may start on SMs this grid's
+  // last CTAs leave idle.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -739,7 +756,11 @@ __global__ void __launch_bounds__(kGradThreads, 1)
   if (warp == kGIssueA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::tmem_cols);
-  }
+    // Started early beside the dK/dV grid: the grid completes only after that
+  // one has, so work after this call sees dK and dV written.
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 }
 
 template <int D>
@@ -752,8 +773,12 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   float* delta = ws.delta;
   const long long rows = (long long)g.BH * g.N;
   constexpr int RPB = 256 / (D / 8);
-  bwd_delta_kernel<D><<<static_cast<unsigned>((rows + RPB - 1) / RPB), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), rows, delta);
+  // D per token, and (two more CTAs) the launch orders of the gradient
+  // kernels: longest lists first, kv-blocks by CSC count, q-blocks by CSR count.
+  const unsigned ndelta = static_cast<unsigned>((rows + RPB - 1) / RPB);
+  bwd_delta_kernel<D><<<ndelta + 2, 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), rows, delta,
+      ndelta, col_cnt, g.BH * g.Mk, ws.col_order, row_cnt, g.BH * g.Mq, ws.row_order);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -763,12 +788,6 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
       make_tmap_bf16(&tdo, dout, g.BH, g.N, D, kBM) != 0)
     return cudaErrorInvalidValue;
   const float scale_log2 = scale * kLog2e;
-
-  // Longest lists first: kv-blocks by CSC count, q-blocks by CSR count.
-  order_by_count_kernel<<<1, kOrderThreads, 0, st>>>(col_cnt, g.BH * g.Mk, ws.col_order);
-  order_by_count_kernel<<<1, kOrderThreads, 0, st>>>(row_cnt, g.BH * g.Mq, ws.row_order);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
 
   e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DkdvCfg<D>::smem_alloc);
@@ -784,10 +803,22 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DqCfg<D>::smem_alloc);
   if (e != cudaSuccess) return e;
-  bwd_dq_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mq), kGradThreads, DqCfg<D>::smem_alloc,
-                     st>>>(tq, tk, tv, tdo, lse, delta, row_idx, row_cnt, ws.row_order, g.N, g.Mq,
-                           g.Mk, scale, scale_log2, static_cast<__nv_bfloat16*>(dq), status);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the dQ CTAs may start while the last dK/dV
+  // CTAs run (D and the launch orders were complete before dK/dV started).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((long long)g.BH * g.Mq));
+  cfg.blockDim = dim3(kGradThreads);
+  cfg.dynamicSmemBytes = DqCfg<D>::smem_alloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D>, tq, tk, tv, tdo, lse,
+                            static_cast<const float*>(delta), row_idx, row_cnt,
+                            static_cast<const int32_t*>(ws.row_order), g.N, g.Mq, g.Mk, scale,
+                            scale_log2, static_cast<__nv_bfloat16*>(dq), status);
 }
 
 }  // namespace
