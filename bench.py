@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per call of each entry point (dram__bytes_read.sum + dram__bytes_write.sum
 # summed over its kernels) from one ncu capture of the default workload (480p, k = 5 %,
 # p = 0) with the current kernels; reported as roofline.traffic on that workload only.
-NCU_TRAFFIC_BYTES = {("wan480", 0.05, 0.0): {"bwd": 1522.9e6, "fwd": 343.9e6, "mask": 214.4e6}}
+NCU_TRAFFIC_BYTES = {("wan480", 0.05, 0.0): {"bwd": 1525.1e6, "fwd": 344.2e6, "mask": 214.5e6}}
 
 
 # ----------------------------------------------------------------------------- helpers
