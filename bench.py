@@ -4,9 +4,12 @@ One step = the whole hot path on one batch of synthetic input: block mask
 (pool + pooled map + hybrid Top-k/Top-p selection + CSC lists), block-sparse
 attention forward, and backward (dQ, dK, dV).  Default workload: the
 Wan2.1-1.3B 480p attention shape, B=1, H=12, N=32760 (21x30x52 latents),
-d=128, 128x64 blocks, k=5% with Top-p off (p=0): exactly 26 of 512 kv-blocks
-per row, 94.92% sparsity.  The hybrid rule at the workload's p=0.9 is timed
-too and reported under "hybrid".
+d=128, 128x64 blocks, k=5% with Top-p off (p=0, the fixed-K point): exactly
+26 of 512 kv-blocks per row, 94.92% sparsity.  The hybrid rule at the
+workload's p=0.9 is timed too ("hybrid"; near-uniform pooled rows keep most
+blocks there), and so is the full step of the local-attention variant of the
+shape at its own rule k=5%, p=0.9, where the hybrid rule reaches about 93%
+sparsity ("hybrid_local").
 
 Prints one JSON line (rank 0).  ``value`` = kept-FLOP TFLOP/s of fwd+bwd
 (algorithmic FLOPs 4*d and 10*d per kept valid query x key pair) divided by
@@ -272,10 +275,20 @@ def run_reference(args, wl, k_frac, p):
     return 0
 
 
+def mask_rule(wl, k_frac, p):
+    mk = -(-wl.N // wl.block_kv)
+    kk = max(1, min(mk, math.ceil(k_frac * mk - 1e-4)))
+    if p <= 0.0:
+        return (f"fixed-K Top-k (p = 0, Top-p off): {kk} of {mk} kv-blocks per row, "
+                f"{1 - kk / mk:.2%} sparsity")
+    return f"hybrid Top-k + Top-p: k = {k_frac:g} (K = {kk} of {mk}), p = {p:g}"
+
+
 def workload_config(wl, k_frac, p, sparsity):
     return {"workload": (f"{wl.name}: Wan2.1-shaped attention fwd+bwd, B={wl.B}, H={wl.H}, "
                          f"N={wl.N} ({'x'.join(map(str, wl.grid))}), d={wl.d}, "
                          f"blocks {wl.block_q}x{wl.block_kv}, k={k_frac:g}, p={p:g}"),
+            "mask_rule": mask_rule(wl, k_frac, p),
             "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "block_q": wl.block_q,
             "block_kv": wl.block_kv, "k_frac": k_frac, "p": p, "sparsity": sparsity,
             "l2": "inputs larger than L2 (Q, K, V, dO: 403 MB per step vs 129 MB L2)"}
@@ -389,7 +402,15 @@ def run_ours(args, wl, k_frac, p):
     ms_step, value = aggregate(ms_step_local, step_flops, 1, distributed)  # all ranks
 
     peaks, peak_kind = load_peaks()
-    tc_peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    # The bf16 peak that matches the run: the burst figure (a GEMM timed alone)
+    # for a timed region under a second, the sustained one (a seconds-long
+    # loop under the power cap) for longer runs; the other is reported beside.
+    burst = float(peaks.get("bf16_tflops", peaks.get("bf16_tflops_sustained")))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    use_burst = total_ms < 1000.0
+    tc_peak = burst if use_burst else sustained
+    tc_other = sustained if use_burst else burst
+    tc_key = "bf16_tflops" if use_burst else "bf16_tflops_sustained"
     hbm_peak = float(peaks["hbm_gbs"])
     roof = {
         "fwd": {"kernel": "sparge_attn_fwd (attn_fwd_kernel)", "bound": "tensor",
@@ -404,8 +425,14 @@ def run_ours(args, wl, k_frac, p):
     }
     for r in roof.values():
         r["frac"] = r["achieved"] / r["peak"]
-        r["peak_source"] = (f"{peak_kind} ({'bf16_tflops_sustained' if r['bound'] == 'tensor' else 'hbm_gbs'}"
-                            f" of MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback")
+        key = tc_key if r["bound"] == "tensor" else "hbm_gbs"
+        r["peak_source"] = (f"{key} of MEASURED_PEAKS.json" if peak_kind == "measured"
+                            else f"fallback {key}")
+        if r["bound"] == "tensor":
+            r["peak_choice"] = (f"{'burst' if use_burst else 'sustained'}: timed region "
+                                f"{total_ms:.0f} ms ({'under' if use_burst else 'over'} 1 s)")
+            r["frac_vs_other_peak"] = {"peak": tc_other,
+                                       "frac": r["achieved"] / tc_other}
     dom = max(part_ms, key=part_ms.get)
     roofline = dict(roof[dom])
     roofline["traffic"] = NCU_TRAFFIC_BYTES.get((wl.name, k_frac, p), {}).get(dom)
@@ -457,6 +484,49 @@ def run_ours(args, wl, k_frac, p):
         hms = e0.elapsed_time(e1) / nh
         hybrid = {"k_frac": k_frac, "p": wl.p, "sparsity": hs, "ms_per_step": hms,
                   "tflops": 14.0 * d * hp / (hms * 1e-3) / 1e12, "steps": nh}
+
+    # The hybrid rule where it reaches high sparsity: the local-attention
+    # variant of the 480p shape (Q and K share a smooth latent field) at its
+    # own rule k = 5 %, p = 0.9, whole step timed (the Top-p search included).
+    local = None
+    if not args.no_hybrid and wl.name == "wan480":
+        lwl = synth.WORKLOADS["wan480_local"]
+        lq, lk, lv, ldo = synth.video_inputs(lwl, device=dev)
+        lo, llse = torch.empty_like(lq), torch.empty_like(lse)
+        lg = tuple(torch.empty_like(lq) for _ in range(3))
+
+        def lstep():
+            r = B.sparge_mask(lq, lk, lwl.k_frac, lwl.p, out=mask_out, workspace=ws_mask)
+            B.sparge_attn_fwd(lq, lk, lv, r["row_idx"], r["row_cnt"], out=lo, lse=llse,
+                              status=status)
+            B.sparge_attn_bwd(lq, lk, lv, lo, llse, ldo, r["row_idx"], r["row_cnt"],
+                              r["col_idx"], r["col_cnt"], out=lg, workspace=ws_bwd,
+                              status=status)
+        lstep()
+        torch.cuda.synchronize()
+        mb = unpack_bits(mask_out["bitmask"], mk)
+        lp = kept_pairs(mb, N, wl.block_q, wl.block_kv)
+        lcnt = mb.sum(-1)
+        ls = 1.0 - float(mb.sum().item()) / float(Bn * H * mq * mk)
+        nl = max(3, min(args.steps, 30))
+        for _ in range(2):
+            lstep()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(nl):
+            lstep()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        lms = e0.elapsed_time(e1) / nl
+        local = {"workload": f"{lwl.name}: the 480p shape with Q, K sharing a smooth latent "
+                             f"field (weight {lwl.rho}, sigma {lwl.shared_sigma}), Q gain "
+                             f"{lwl.q_gain}",
+                 "k_frac": lwl.k_frac, "p": lwl.p, "sparsity": ls,
+                 "kept_per_row": {"min": int(lcnt.min()), "median": float(lcnt.float().median()),
+                                  "max": int(lcnt.max())},
+                 "ms_per_step": lms, "tflops": 14.0 * d * lp / (lms * 1e-3) / 1e12, "steps": nl}
+        del lq, lk, lv, ldo, lo, llse, lg
+        torch.cuda.empty_cache()
 
     # End to end through the public API, as a user would stream batches: per step
     # the H2D copy of that step's Q, K, V, dO from pinned host memory, the step,
@@ -541,6 +611,7 @@ def run_ours(args, wl, k_frac, p):
             "roofline_all": roof,
             "mask_alone": mask_alone,
             "hybrid": hybrid,
+            "hybrid_local": local,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -642,7 +713,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="wan480", choices=("wan480", "wan720", "wan480_d64"))
+    ap.add_argument("--workload", default="wan480",
+                    choices=("wan480", "wan720", "wan480_d64", "wan480_local"))
     ap.add_argument("--k-frac", type=float, default=None)
     ap.add_argument("--p", type=float, default=0.0, help="Top-p of the headline step (0 = off)")
     ap.add_argument("--no-hybrid", action="store_true")

@@ -73,15 +73,15 @@ _SIGNATURES = {
     "sparge_pool": ([_SHP, _P, _P, _P, _P, _P], _I),
     "sparge_mask_workspace_bytes": ([_SHP, ctypes.POINTER(_SZ)], _I),
     "sparge_mask": ([_SHP, _P, _P, _F, _F, _F, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
-    "sparge_mask_from_prob": ([_SHP, _P, _F, _F, _P, _P, _P, _P, _P, _P, _P], _I),
+    "sparge_mask_from_prob": ([_SHP, _P, _F, _F, _P, _P, _P, _P, _P, _P], _I),
     "sparge_mask_noalloc": ([_SHP, _P, _P, _F, _F, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "sparge_attn_fwd": ([_SHP, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P], _I),
     "sparge_attn_bwd_workspace_bytes": ([_SHP, ctypes.POINTER(_SZ)], _I),
     "sparge_attn_bwd": ([_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P, _SZ,
                          _P, _P], _I),
+    "sparge_status_copy_async": ([_P, _P, _P], _I),
     "sparge_read_status": ([_P, _P, ctypes.POINTER(ctypes.c_int32)], _I),
     "sparge_debug_wait_probe": ([_P, ctypes.c_uint64, _P], _I),
-    "sparge_debug_exp2_poly": ([_P, _P, _I, _P], _I),
 }
 
 _lib = None
@@ -216,7 +216,7 @@ def sparge_mask(q, k, k_frac: float, p: float, softmax_scale: float = 0.0, want_
     _check(lib.sparge_mask(ctypes.byref(shp), _ptr(q), _ptr(k), float(k_frac), float(p),
                            float(softmax_scale), _ptr(res["bitmask"]), _ptr(res["row_idx"]),
                            _ptr(res["row_cnt"]), _ptr(res["col_idx"]), _ptr(res["col_cnt"]),
-                           _ptr(res["logit"]), _ptr(res["prob"]), _ptr(workspace),
+                           _ptr(res["prob"]), _ptr(res["logit"]), _ptr(workspace),
                            workspace.numel(), None, _stream(q.device)), "sparge_mask")
     return res
 
@@ -235,7 +235,7 @@ def sparge_mask_from_prob(prob: torch.Tensor, k_frac: float, p: float, N: int, d
     _check(lib.sparge_mask_from_prob(ctypes.byref(shp), _ptr(prob), float(k_frac), float(p),
                                      _ptr(res["bitmask"]), _ptr(res["row_idx"]),
                                      _ptr(res["row_cnt"]), _ptr(res["col_idx"]),
-                                     _ptr(res["col_cnt"]), None, _stream(prob.device)),
+                                     _ptr(res["col_cnt"]), _stream(prob.device)),
            "sparge_mask_from_prob")
     return res
 
@@ -281,16 +281,6 @@ def sparge_attn_bwd(q, k, v, o, lse, dout, row_idx, row_cnt, col_idx, col_cnt,
            "sparge_attn_bwd")
     _finish(st, check_status, "sparge_attn_bwd")
     return dq, dk, dv
-
-
-def sparge_debug_exp2_poly(x: torch.Tensor) -> torch.Tensor:
-    """2^x by the library's FMA-pipe polynomial (for testing it)."""
-    if not (x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
-        raise ValueError("x must be a contiguous fp32 CUDA tensor")
-    y = torch.empty_like(x)
-    _check(load_library().sparge_debug_exp2_poly(_ptr(x), _ptr(y), x.numel(), _stream(x.device)),
-           "sparge_debug_exp2_poly")
-    return y
 
 
 def sparge_debug_wait_probe(timeout_ns: int = 10_000_000, device="cuda") -> int:

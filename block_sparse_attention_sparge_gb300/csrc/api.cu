@@ -110,16 +110,33 @@ __global__ void wait_probe_kernel(int32_t* status, uint64_t timeout_ns) {
   if (!mbar_wait(b, 0, timeout_ns)) report_error(status, SPARGE_ERR_TIMEOUT);
 }
 
-__global__ void exp2_poly_kernel(const float* __restrict__ x, float* __restrict__ y, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) y[i] = exp2_poly(x[i]);
-}
-
 }  // namespace
 
 cudaError_t launch_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t st) {
   wait_probe_kernel<<<1, 32, 0, st>>>(status, timeout_ns);
   return cudaGetLastError();
+}
+
+int validate_mask_args(const sparge_shape* shape, const void* q, const void* k, float k_frac,
+                       float p, float softmax_scale, const uint32_t* bitmask,
+                       const int32_t* row_idx, const int32_t* row_cnt, const int32_t* col_idx,
+                       const int32_t* col_cnt, const float* pooled_prob,
+                       const float* pooled_logit, const int32_t* status) {
+  SPARGE_TRY(check_shape(shape));
+  SPARGE_TRY(check_tensor(q));
+  SPARGE_TRY(check_tensor(k));
+  SPARGE_TRY(check_kp(k_frac, p));
+  SPARGE_TRY(check_opt_word(status));
+  if (!isfinite(softmax_scale)) return SPARGE_ERR_INVALID_ARG;
+  SPARGE_TRY(check_word(bitmask));
+  SPARGE_TRY(check_word(row_idx));
+  SPARGE_TRY(check_word(row_cnt));
+  if ((col_idx == nullptr) != (col_cnt == nullptr)) return SPARGE_ERR_INVALID_ARG;
+  SPARGE_TRY(check_opt_word(col_idx));
+  SPARGE_TRY(check_opt_word(col_cnt));
+  SPARGE_TRY(check_opt_word(pooled_prob));
+  SPARGE_TRY(check_opt_word(pooled_logit));
+  return SPARGE_OK;
 }
 
 }  // namespace sparge
@@ -164,22 +181,10 @@ int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes) {
 
 int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k_frac, float p,
                 float softmax_scale, uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
-                int32_t* col_idx, int32_t* col_cnt, float* pooled_logit, float* pooled_prob,
+                int32_t* col_idx, int32_t* col_cnt, float* pooled_prob, float* pooled_logit,
                 void* workspace, size_t ws_bytes, int32_t* status, sparge_stream_t stream) {
-  SPARGE_TRY(check_shape(shape));
-  SPARGE_TRY(check_tensor(q));
-  SPARGE_TRY(check_tensor(k));
-  SPARGE_TRY(check_kp(k_frac, p));
-  SPARGE_TRY(check_opt_word(status));
-  if (!isfinite(softmax_scale)) return SPARGE_ERR_INVALID_ARG;
-  SPARGE_TRY(check_word(bitmask));
-  SPARGE_TRY(check_word(row_idx));
-  SPARGE_TRY(check_word(row_cnt));
-  if ((col_idx == nullptr) != (col_cnt == nullptr)) return SPARGE_ERR_INVALID_ARG;
-  SPARGE_TRY(check_opt_word(col_idx));
-  SPARGE_TRY(check_opt_word(col_cnt));
-  SPARGE_TRY(check_opt_word(pooled_logit));
-  SPARGE_TRY(check_opt_word(pooled_prob));
+  SPARGE_TRY(validate_mask_args(shape, q, k, k_frac, p, softmax_scale, bitmask, row_idx, row_cnt,
+                                col_idx, col_cnt, pooled_prob, pooled_logit, status));
   const Geom g = make_geom(*shape);
   if (workspace == nullptr || ws_bytes < mask_ws_bytes(g)) return SPARGE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SPARGE_ERR_MISALIGNED;
@@ -201,9 +206,7 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
 
 int sparge_mask_from_prob(const sparge_shape* shape, const float* prob, float k_frac, float p,
                           uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
-                          int32_t* col_idx, int32_t* col_cnt, int32_t* status,
-                          sparge_stream_t stream) {
-  (void)status;
+                          int32_t* col_idx, int32_t* col_cnt, sparge_stream_t stream) {
   SPARGE_TRY(check_shape(shape));
   SPARGE_TRY(check_word(prob));
   SPARGE_TRY(check_kp(k_frac, p));
@@ -274,6 +277,13 @@ int sparge_attn_bwd(const sparge_shape* shape, const void* q, const void* k, con
                                      status, stream));
 }
 
+int sparge_status_copy_async(const int32_t* status, int32_t* host_status, sparge_stream_t stream) {
+  SPARGE_TRY(check_word(status));
+  if (host_status == nullptr) return SPARGE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemcpyAsync(host_status, status, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                     stream));
+}
+
 int sparge_read_status(const int32_t* status, sparge_stream_t stream, int32_t* host_status) {
   SPARGE_TRY(check_word(status));
   if (host_status == nullptr) return SPARGE_ERR_INVALID_ARG;
@@ -283,15 +293,6 @@ int sparge_read_status(const int32_t* status, sparge_stream_t stream, int32_t* h
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SPARGE_ERR_CUDA;
   *host_status = h;
   return SPARGE_OK;
-}
-
-int sparge_debug_exp2_poly(const float* x, float* y, int n, sparge_stream_t stream) {
-  SPARGE_TRY(check_word(x));
-  SPARGE_TRY(check_word(y));
-  if (n < 0) return SPARGE_ERR_INVALID_ARG;
-  if (n == 0) return SPARGE_OK;
-  exp2_poly_kernel<<<(n + 255) / 256, 256, 0, stream>>>(x, y, n);
-  return cuda_status(cudaGetLastError());
 }
 
 int sparge_debug_wait_probe(int32_t* status, uint64_t timeout_ns, sparge_stream_t stream) {

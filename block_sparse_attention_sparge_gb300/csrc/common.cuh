@@ -252,20 +252,6 @@ SPARGE_DEV float ex2_approx(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, to take load off the special-function unit.  Split
-// x = i + f with i = floor(x) and f in [0, 1); 2^f is a cubic whose
-// coefficients were fitted here by weighted least squares on [0, 1) (max
-// relative error 8.6e-5, far below bf16 resolution), and 2^i is added to the
-// exponent field.  Results below 2^-126 (and x = -inf) flush to 0.
-SPARGE_DEV float exp2_poly(float x) {
-  const float xc = fmaxf(x, -126.f);
-  const float fi = floorf(xc);
-  const float f = xc - fi;
-  const float p = fmaf(fmaf(fmaf(0.07706708f, f, 0.22764495f), f, 0.6951168f), f, 1.0f);
-  const float r = __int_as_float(__float_as_int(p) + (static_cast<int>(fi) << 23));
-  return x < -126.f ? 0.f : r;
-}
-
 SPARGE_DEV uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
 }  // namespace sparge

@@ -61,6 +61,12 @@ cudaError_t launch_attn_bwd(const Geom& g, const void* q, const void* k, const v
 
 // api.cu
 cudaError_t launch_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t st);
+// Every argument check of sparge_mask (no CUDA call); SPARGE_OK or the error.
+int validate_mask_args(const sparge_shape* shape, const void* q, const void* k, float k_frac,
+                       float p, float softmax_scale, const uint32_t* bitmask,
+                       const int32_t* row_idx, const int32_t* row_cnt, const int32_t* col_idx,
+                       const int32_t* col_cnt, const float* pooled_prob,
+                       const float* pooled_logit, const int32_t* status);
 
 // tma.cu: 3-D bf16 tensor map over [BH, N, d] with a (64 x box_rows) 128-byte-swizzled box.
 int make_tmap_bf16(void* tmap_out, const void* base, int BH, int N, int d, int box_rows);

@@ -16,9 +16,10 @@ no dataset, prompt or weight is used):
 The video-shaped Q and K are spatially smooth Gaussian fields: white noise on
 the (t, h, w) grid convolved with a separable Gaussian (sigma = 1, 3, 3
 tokens, truncated at 3 sigma, zero padding), then each (head, channel)
-restandardised to mean 0 and std 1.  Q and K are independent fields (an
-optional ``rho`` > 0 mixes in a latent field shared by Q and K; the default
-is 0).  Four sink tokens (0..3) get a strong common direction ``u`` (unit
+restandardised to mean 0 and std 1.  Q and K are independent fields, except
+in ``wan480_local``, where a latent field shared by Q and K (weight ``rho``,
+its own smoothing) is mixed into both and Q is scaled by ``q_gain``.  Four
+sink tokens (0..3) get a strong common direction ``u`` (unit
 vector, per head) in K, and every query gets a weak component along ``u``:
 K_s += 3 sqrt(d) u for s < 4, Q_t += 0.25 sqrt(d) u for all t, a token-level
 logit margin of 0.75 sqrt(d).  V and dO are white N(0, 1).
@@ -26,7 +27,9 @@ Seeds: Q 1, K 2, V 3, dO 4, sink directions 5, shared latent 7.
 
 Independent smooth fields give near-uniform pooled rows (pooled logit std
 about 0.2 at the 480p shape), so Top-p at p = 0.9 keeps most blocks there;
-a Top-k-only mask (p = 0) gives the 95% sparsity point.
+a Top-k-only mask (p = 0) gives the 95% sparsity point.  The shared latent
+of ``wan480_local`` makes each pooled row peak around its own neighbourhood,
+so there the hybrid rule itself reaches high sparsity.
 """
 
 from __future__ import annotations
@@ -58,6 +61,9 @@ class Workload:
     block_kv: int = 64
     k_frac: float = 0.05
     p: float = 0.9
+    rho: float = 0.0              # weight of the latent field shared by Q and K
+    shared_sigma: tuple = (1.0, 3.0, 3.0)  # smoothing of that shared field
+    q_gain: float = 1.0           # Q is scaled by this before the sinks are added
 
     @property
     def N(self) -> int:
@@ -71,11 +77,16 @@ WORKLOADS = {
     # The 480p token grid with head width 64 (24 heads: the same model width):
     # the d = 64 variant of the kernels at full size.
     "wan480_d64": Workload("wan480_d64", 1, 24, (21, 30, 52), 64, 128, 64, 0.05, 0.9),
+    # The 480p shape with local attention: Q and K share a smoother latent
+    # field (sigma 2, 8, 8 tokens; weight 0.9) and Q carries a gain of 2.5, so
+    # each pooled row peaks around its own neighbourhood and the hybrid rule at
+    # k = 5 %, p = 0.9 keeps few blocks, with uneven counts per row.
+    "wan480_local": Workload("wan480_local", 1, 12, (21, 30, 52), 128, 128, 64, 0.05, 0.9,
+                             rho=0.9, shared_sigma=(2.0, 8.0, 8.0), q_gain=2.5),
 }
 
 # Generator constants (fixed once; recorded in the design notes).
 SIGMA = (1.0, 3.0, 3.0)
-RHO = 0.0            # weight of an optional latent field shared by Q and K
 SINK_TOKENS = 4
 SINK_K_GAIN = 3.0    # K_s += SINK_K_GAIN * sqrt(d) * u for s < SINK_TOKENS
 SINK_Q_GAIN = 0.25   # Q_t += SINK_Q_GAIN * sqrt(d) * u for every t
@@ -104,11 +115,11 @@ def _smooth_axis(x: torch.Tensor, axis: int, sigma: float) -> torch.Tensor:
     return y.reshape(shp).movedim(-1, axis)
 
 
-def _smooth_field(H: int, grid, d: int, seed: int, device) -> torch.Tensor:
+def _smooth_field(H: int, grid, d: int, seed: int, device, sigma=SIGMA) -> torch.Tensor:
     """[H, N, d] fp32 smooth field, each (head, channel) mean 0, std 1."""
     g = _gen(seed, device)
     x = torch.randn((H,) + tuple(grid) + (d,), generator=g, device=device, dtype=torch.float32)
-    for ax, s in zip((1, 2, 3), SIGMA):
+    for ax, s in zip((1, 2, 3), sigma):
         x = _smooth_axis(x, ax, s)
     x = x.reshape(H, -1, d)
     x = x - x.mean(dim=1, keepdim=True)
@@ -124,7 +135,7 @@ def tiny_inputs(device="cpu", seed: int = 0, H: int = 2, N: int = 1024, d: int =
     return tuple(out)
 
 
-def video_inputs(wl: Workload, device="cpu", heads=None, rho: float = RHO):
+def video_inputs(wl: Workload, device="cpu", heads=None, rho=None):
     """Video-shaped Q, K, V, dO bf16 [B, H, N, d] (B = 1); see the module docstring.
 
     ``heads`` (optional) limits generation to the first ``heads`` heads: each
@@ -133,13 +144,16 @@ def video_inputs(wl: Workload, device="cpu", heads=None, rho: float = RHO):
     """
     H = wl.H if heads is None else int(heads)
     d, N = wl.d, wl.N
+    rho = wl.rho if rho is None else float(rho)
     q = _smooth_field(H, wl.grid, d, 1, device)
     k = _smooth_field(H, wl.grid, d, 2, device)
     if rho > 0.0:
-        shared = _smooth_field(H, wl.grid, d, 7, device)
+        shared = _smooth_field(H, wl.grid, d, 7, device, sigma=wl.shared_sigma)
         a = math.sqrt(max(0.0, 1.0 - rho * rho))
         q = rho * shared + a * q
         k = rho * shared + a * k
+    if wl.q_gain != 1.0:
+        q = wl.q_gain * q
     gu = _gen(5, device)
     u = torch.randn((H, d), generator=gu, device=device, dtype=torch.float32)
     u = u / u.norm(dim=1, keepdim=True)

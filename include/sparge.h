@@ -14,16 +14,17 @@
  * - Blocks: block_q query tokens by block_kv key tokens.  Mq = ceil(N/block_q),
  *   Mk = ceil(N/block_kv).  The last block of each may be partial.
  * - The caller owns every buffer and the stream.  The library allocates,
- *   frees and synchronises nothing (sparge_read_status excepted, which
- *   synchronises the given stream), and keeps no global mutable state apart
- *   from the fixed scratch array of sparge_mask_noalloc.
+ *   frees and synchronises nothing, and keeps no global mutable state apart
+ *   from the fixed scratch array of sparge_mask_noalloc.  The one blocking
+ *   call is sparge_read_status, a convenience that synchronises the given
+ *   stream; sparge_status_copy_async reads the same word without blocking.
  * - All launches are asynchronous on `stream` (NULL = the legacy default
  *   stream).  Arguments are validated before any launch; on an error nothing
  *   is launched and a negative status is returned.
  * - `status` (nullable) is a device int32 the caller zeroes before use.  A
  *   kernel that gives up on a bounded internal wait writes SPARGE_ERR_TIMEOUT
  *   there (first error wins) and returns instead of hanging.  Read it with
- *   sparge_read_status.
+ *   sparge_status_copy_async (stream-ordered) or sparge_read_status.
  * - softmax_scale 0 means 1/sqrt(d).
  */
 #ifndef SPARGE_H_
@@ -103,8 +104,8 @@ int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes);
  *   col_idx/cnt  : int32 [B,H,Mk,Mq] / [B,H,Mk] out; the transposed lists
  *                  (kept q-blocks per kv-block, ascending).  Both NULL or both
  *                  set; needed by sparge_attn_bwd.
- *   pooled_logit : fp32 [B,H,Mq,Mk] out, L (nullable).
  *   pooled_prob  : fp32 [B,H,Mq,Mk] out, P (nullable).
+ *   pooled_logit : fp32 [B,H,Mq,Mk] out, L (nullable).
  *   workspace    : device buffer of sparge_mask_workspace_bytes bytes (pooled
  *                  Q and K, pooled logits; no initial contents needed),
  *                  16-byte aligned.
@@ -119,7 +120,7 @@ int sparge_mask_workspace_bytes(const sparge_shape* shape, size_t* bytes);
  */
 int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k_frac, float p,
                 float softmax_scale, uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
-                int32_t* col_idx, int32_t* col_cnt, float* pooled_logit, float* pooled_prob,
+                int32_t* col_idx, int32_t* col_cnt, float* pooled_prob, float* pooled_logit,
                 void* workspace, size_t ws_bytes, int32_t* status, sparge_stream_t stream);
 
 /*
@@ -133,8 +134,11 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
  *   the library, one per GPU that loads it, kept until the process exits.
  *   Shapes whose workspace (sparge_mask_workspace_bytes) exceeds 16 MiB return
  *   SPARGE_ERR_WORKSPACE before any launch.
- *   The first call on a device (made with that device current) looks up the
- *   array's device address once; make that first call before any stream
+ *   Every argument is checked before any CUDA call.  The first call in a
+ *   CUDA context (the current one: normally the primary context of the
+ *   current device) looks up the array's device address in that context and
+ *   caches it by the context's unique id, so a device reset or another
+ *   context gets a fresh lookup; make that first call before any stream
  *   capture.  It allocates nothing: no cudaMalloc, cudaFree or allocating
  *   library routine.
  *   Every call on a device shares the one array, which keeps the last call's
@@ -145,7 +149,7 @@ int sparge_mask(const sparge_shape* shape, const void* q, const void* k, float k
 int sparge_mask_noalloc(const sparge_shape* shape, const void* q, const void* k, float k_frac,
                         float p, float softmax_scale, uint32_t* bitmask, int32_t* row_idx,
                         int32_t* row_cnt, int32_t* col_idx, int32_t* col_cnt,
-                        float* pooled_logit, float* pooled_prob, int32_t* status,
+                        float* pooled_prob, float* pooled_logit, int32_t* status,
                         sparge_stream_t stream);
 
 /*
@@ -157,8 +161,7 @@ int sparge_mask_noalloc(const sparge_shape* shape, const void* q, const void* k,
  */
 int sparge_mask_from_prob(const sparge_shape* shape, const float* prob, float k_frac, float p,
                           uint32_t* bitmask, int32_t* row_idx, int32_t* row_cnt,
-                          int32_t* col_idx, int32_t* col_cnt, int32_t* status,
-                          sparge_stream_t stream);
+                          int32_t* col_idx, int32_t* col_cnt, sparge_stream_t stream);
 
 /*
  * sparge_attn_fwd -- block-sparse attention forward, step 4.
@@ -207,7 +210,14 @@ int sparge_attn_bwd(const sparge_shape* shape, const void* q, const void* k, con
                     float softmax_scale, void* dq, void* dk, void* dv, void* workspace,
                     size_t ws_bytes, int32_t* status, sparge_stream_t stream);
 
-/* Copies the device status word to *host_status after synchronising `stream`. */
+/* Enqueues on `stream` a copy of the device status word into *host_status
+ * (caller-owned, page-locked host memory for the copy to be asynchronous) and
+ * returns without waiting; the value is valid once the stream has reached the
+ * copy (e.g. after an event the caller records behind it completes). */
+int sparge_status_copy_async(const int32_t* status, int32_t* host_status, sparge_stream_t stream);
+
+/* Blocking convenience: copies the device status word to *host_status and
+ * synchronises `stream` before returning (the library's one blocking call). */
 int sparge_read_status(const int32_t* status, sparge_stream_t stream, int32_t* host_status);
 
 /*
@@ -217,14 +227,6 @@ int sparge_read_status(const int32_t* status, sparge_stream_t stream, int32_t* h
  * path that never hangs the GPU.
  */
 int sparge_debug_wait_probe(int32_t* status, uint64_t timeout_ns, sparge_stream_t stream);
-
-/*
- * sparge_debug_exp2_poly -- y[i] = 2^x[i] by the FMA-pipe polynomial the
- * attention kernels can use for part of their exponentials (x = i + f,
- * fitted cubic for 2^f, relative error < 1e-4; values below 2^-126 flush to
- * 0).  For testing that routine against CUDA's exp2.  x, y: fp32 device, n >= 0.
- */
-int sparge_debug_exp2_poly(const float* x, float* y, int n, sparge_stream_t stream);
 
 #ifdef __cplusplus
 }

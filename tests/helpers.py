@@ -49,3 +49,40 @@ def mask_to_csc_tensors(mask: np.ndarray, device):
 
 def rel_l2(a: np.ndarray, b: np.ndarray) -> float:
     return float(np.linalg.norm((a - b).ravel()) / max(np.linalg.norm(b.ravel()), 1e-30))
+
+
+def check_fwd_heads(q, k, v, mask, o, lse, heads, bq=128, bk=64, tag=""):
+    """Every row of the listed heads (b = 0) against the fp32 block-gather
+    oracle, element by element: O within the max-abs and relative-L2 bounds,
+    LSE within LSE_ATOL (both -inf exactly where a q-block keeps nothing)."""
+    import oracle as O
+    for h in heads:
+        sl = slice(h, h + 1)
+        o_ref, lse_ref = O.sparse_attention_blocks(
+            to_np(q[:, sl], np.float32), to_np(k[:, sl], np.float32),
+            to_np(v[:, sl], np.float32), mask[:, sl], bq, bk, dtype=np.float32)
+        o_g = to_np(o[:, sl])
+        err = float(np.abs(o_g - o_ref).max())
+        rl = rel_l2(o_g, o_ref)
+        assert err <= O_MAX_ABS and rl <= O_REL_L2, (tag, h, err, rl)
+        lg = to_np(lse[:, sl])
+        fin = np.isfinite(lse_ref)
+        np.testing.assert_array_equal(np.isneginf(lg), ~fin)
+        np.testing.assert_allclose(lg[fin], lse_ref[fin], atol=LSE_ATOL, rtol=0)
+
+
+def check_bwd_heads(q, k, v, do, mask, grads, heads, bq=128, bk=64, tag=""):
+    """dQ, dK, dV of the listed heads (b = 0) within GRAD_REL_L2 of the fp32
+    block-gather oracle."""
+    import oracle as O
+    for h in heads:
+        sl = slice(h, h + 1)
+        refs = O.sparse_attention_blocks_bwd(
+            to_np(q[:, sl], np.float32), to_np(k[:, sl], np.float32),
+            to_np(v[:, sl], np.float32), to_np(do[:, sl], np.float32), mask[:, sl], bq, bk,
+            dtype=np.float32)
+        for name, g, r in zip(("dq", "dk", "dv"), grads, refs):
+            gn = to_np(g[:, sl])
+            assert np.isfinite(gn).all(), (tag, h, name)
+            rl = rel_l2(gn, r)
+            assert rl <= GRAD_REL_L2, (tag, h, name, rl)

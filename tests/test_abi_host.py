@@ -130,7 +130,33 @@ def test_fwd_bwd_argument_validation(lib):
     assert lib.sparge_attn_bwd(ctypes.byref(s), *args, 0.0, None, FAKE, FAKE, FAKE,
                                ctypes.c_size_t(1 << 30), None, None) == B.SPARGE_ERR_INVALID_ARG
     assert lib.sparge_read_status(None, None, None) == B.SPARGE_ERR_INVALID_ARG
+    assert lib.sparge_status_copy_async(None, None, None) == B.SPARGE_ERR_INVALID_ARG
+    assert lib.sparge_status_copy_async(FAKE, None, None) == B.SPARGE_ERR_INVALID_ARG
     assert lib.sparge_debug_wait_probe(None, 10, None) == B.SPARGE_ERR_INVALID_ARG
+
+
+def test_noalloc_checks_arguments_before_any_cuda_call(lib):
+    """The allocation-free mask entry point validates every argument before it
+    touches CUDA (here, with no GPU, any CUDA call would fail differently)."""
+    s = _shape()
+    args = dict(q=FAKE, k=FAKE, kf=0.1, p=0.9, scale=0.0, bm=FAKE, ri=FAKE, rc=FAKE, ci=None,
+                cc=None, pr=None, lg=None, st=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.sparge_mask_noalloc(ctypes.byref(s), a["q"], a["k"], a["kf"], a["p"],
+                                       a["scale"], a["bm"], a["ri"], a["rc"], a["ci"], a["cc"],
+                                       a["pr"], a["lg"], a["st"], None)
+    assert call(q=None) == B.SPARGE_ERR_INVALID_ARG
+    assert call(k=ODD) == B.SPARGE_ERR_MISALIGNED
+    assert call(kf=0.0) == B.SPARGE_ERR_INVALID_ARG
+    assert call(p=2.0) == B.SPARGE_ERR_INVALID_ARG
+    assert call(bm=None) == B.SPARGE_ERR_INVALID_ARG
+    assert call(ci=FAKE) == B.SPARGE_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == B.SPARGE_ERR_INVALID_ARG
+    big = B.Shape(1, 40, 75600, 128, 128, 64)
+    assert lib.sparge_mask_noalloc(ctypes.byref(big), FAKE, FAKE, 0.05, 0.9, 0.0, FAKE, FAKE, FAKE,
+                                   None, None, None, None, None, None) == B.SPARGE_ERR_WORKSPACE
 
 
 def test_binding_fails_loudly_without_cuda_tensors():

@@ -1,8 +1,8 @@
 """The d = 64 kernels at full size: the 480p token grid (N = 32760 =
 21x30x52) with 24 heads of width 64, blocks 128x64 (Mq = 256, Mk = 512), in the
 launch configuration the benchmark uses (``--workload wan480_d64``).  The mask
-is bit-exact on the GPU's P for every row, forward rows are sampled on two
-heads, and dQ, dK, dV of two heads are checked against the fp32 oracle."""
+is bit-exact on the GPU's P for every row; every row of the forward (O and LSE)
+of two heads and their dQ, dK, dV are checked against the fp32 oracle."""
 
 import numpy as np
 import pytest
@@ -11,8 +11,7 @@ import torch
 import oracle as O
 from block_sparse_attention_sparge_gb300 import binding as B
 from block_sparse_attention_sparge_gb300 import synth
-from helpers import (GRAD_REL_L2, LSE_ATOL, MAP_ATOL, O_MAX_ABS, O_REL_L2, rel_l2, to_np,
-                     unpack_bitmask)
+from helpers import MAP_ATOL, check_bwd_heads, check_fwd_heads, to_np, unpack_bitmask
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -39,17 +38,5 @@ def test_d64_full_size(wan480_d64, k_frac, p):
     got = unpack_bitmask(res["bitmask"], MK)
     assert (got == ref).all()
     np.testing.assert_array_equal(res["row_cnt"].cpu().numpy(), ref.sum(-1))
-    rows = np.r_[0:4, 16380:16384, 32700:32760:11, 32759]
-    for h in HEADS:
-        sl = slice(h, h + 1)
-        o_ref, lse_ref = O.sparse_attention_rows(to_np(q[:, sl]), to_np(k[:, sl]), to_np(v[:, sl]),
-                                                 ref[:, sl], 128, 64, 0, 0, rows)
-        o_g = to_np(o[0, h, rows])
-        err = np.abs(o_g - o_ref).max()
-        assert err <= O_MAX_ABS and rel_l2(o_g, o_ref) <= O_REL_L2, (h, err)
-        np.testing.assert_allclose(to_np(lse[0, h, rows]), lse_ref, atol=LSE_ATOL, rtol=0)
-        refs = O.sparse_attention_blocks_bwd(
-            to_np(q[:, sl], np.float32), to_np(k[:, sl], np.float32), to_np(v[:, sl], np.float32),
-            to_np(do[:, sl], np.float32), ref[:, sl], 128, 64, dtype=np.float32)
-        for name, g, r in zip(("dq", "dk", "dv"), (dq[:, sl], dk[:, sl], dv[:, sl]), refs):
-            assert rel_l2(to_np(g), r) <= GRAD_REL_L2, (h, name)
+    check_fwd_heads(q, k, v, ref, o, lse, HEADS, tag=f"d64 k={k_frac} p={p}")
+    check_bwd_heads(q, k, v, do, ref, (dq, dk, dv), HEADS, tag=f"d64 k={k_frac} p={p}")

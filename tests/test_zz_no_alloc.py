@@ -39,8 +39,8 @@ def _noalloc_mask(q, k, k_frac, p):
     shp = B.Shape(Bn, H, N, d, 128, 64)
     rc = lib.sparge_mask_noalloc(ctypes.byref(shp), _ptr(q), _ptr(k), float(k_frac), float(p), 0.0,
                                  _ptr(out["bitmask"]), _ptr(out["row_idx"]), _ptr(out["row_cnt"]),
-                                 _ptr(out["col_idx"]), _ptr(out["col_cnt"]), _ptr(out["logit"]),
-                                 _ptr(out["prob"]), None,
+                                 _ptr(out["col_idx"]), _ptr(out["col_cnt"]), _ptr(out["prob"]),
+                                 _ptr(out["logit"]), None,
                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == B.SPARGE_OK, B.status_string(rc)
     return out
