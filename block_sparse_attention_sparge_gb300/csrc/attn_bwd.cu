@@ -11,24 +11,30 @@
 // with D_t = sum_c dO_tc O_tc.
 //
 // Kernels, no atomics (deterministic):
-//   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads).
-//   (two extra CTAs of the delta grid) launch orders of the two gradient
-//                     kernels: long lists first, then index order (a stable
-//                     partition).
-//   bwd_dkdv_kernel   one CTA per kv-block, loops over the q-blocks that keep
-//                     it (CSC list).  S and dP are recomputed into TMEM
-//                     (M = 128 query rows); dV^T and dK^T accumulate in TMEM
-//                     as M = d tiles, dV^T += dO^T P and dK^T += Q^T dS, with
-//                     dO, Q, P and dS read in the MN-major smem layout.
-//   bwd_dq_kernel     one CTA per q-block, loops over its kept kv-blocks (CSR
-//                     list); recomputes S, dP and dS and accumulates
-//                     dQ += dS K in TMEM.  Q and dO (reused by every tile)
-//                     and dS are MMA A operands read from TMEM.
-// Roles per CTA: eight compute warps (two per TMEM lane quarter, each owning
-// 32 of a tile's 64 key columns), a TMA producer warp and two MMA-issuing
-// warps (S and dP; then the gradient MMAs; two issuers let the gradient MMAs
-// of a tile be queued while the next tile's S and dP are issued).  Every wait
-// is bounded.
+//   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads); two extra CTAs
+//                     build the launch orders of the gradient kernels (long
+//                     work lists first, then index order: a stable partition).
+//   bwd_dkdv_kernel   one CTA per pair of adjacent 64-key kv-blocks (128 keys,
+//                     one 128-key block when block_kv = 128).  The keys are
+//                     the M = 128 rows of every MMA: S^T = K Q^T and
+//                     dP^T = V dO^T land in TMEM with a key per lane, the
+//                     compute warps turn them into P^T and dS^T in place
+//                     (bf16), and those are the A operands, read from TMEM,
+//                     of dV += P^T dO and dK += dS^T Q.  The CTA walks the
+//                     union of the two blocks' column lists; a q-block that
+//                     keeps only one of the two gets zero P and dS in the
+//                     other block's rows.  Each q-block is processed as two
+//                     halves of 64 queries, so that the S/dP tiles of one half
+//                     are computed while the compute warps work on the other
+//                     half and its gradients run.
+//   bwd_dq_kernel     one CTA per q-block; its kept kv-blocks are taken two at
+//                     a time (N = 128 keys per MMA): S = Q K^T (double-buffered
+//                     in TMEM) and dP = dO V^T with Q and dO in shared memory,
+//                     dS written in place over S (bf16), dQ += dS K
+//                     accumulated in TMEM.
+// Every MMA is M = 128 with N >= 64 (the 64-query halves of the dK/dV kernel)
+// or N = 128.  Roles per CTA: compute warps, a TMA producer warp and two
+// MMA-issuing warps.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,28 +48,28 @@ namespace sparge {
 
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 64;
+constexpr int kBM = 128;    // q-block rows
+constexpr int kBN = 64;     // rows of one TMA box of K / V (a 64-key kv-block)
+constexpr int kPair = 128;  // keys per gradient tile (two 64-key boxes)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- work order
-// Launch order of the gradient CTAs: the lists longer than twice the mean
-// first, then the others, each group in index order (a stable partition).
-// Long lists (attention-sink blocks that nearly every q-block keeps) would
-// otherwise run alone at the end of the grid; index order keeps the CTAs of
-// one head together, so that head's Q/dO (or K/V) tiles are served from L2.
-// One CTA of NT threads partitions the n items.
-template <int NT>
-__device__ void order_by_count(const int32_t* __restrict__ cnt, int n, int32_t* __restrict__ order) {
+// Launch order of the gradient CTAs: the items whose work is longer than twice
+// the mean first, then the others, each group in index order (a stable
+// partition).  Long lists (attention-sink blocks that nearly every q-block
+// keeps) would otherwise run alone at the end of the grid; index order keeps
+// the CTAs of one head together, so that head's tiles are served from L2.
+// One CTA of NT threads partitions the n items; work(it) gives an item's size.
+template <int NT, typename Work>
+__device__ void order_by_work(int n, Work work, int32_t* __restrict__ order) {
   constexpr int W = NT / 32;
   __shared__ long long red[W];
   __shared__ int scan[W];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int E = (n + NT - 1) / NT;
   const int lo = min(n, tid * E), hi = min(n, lo + E);
-  // Total of the counts.
   long long sum = 0;
-  for (int it = lo; it < hi; ++it) sum += max(__ldg(cnt + it), 0);
+  for (int it = lo; it < hi; ++it) sum += work(it);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane == 0) red[w] = sum;
@@ -71,11 +77,10 @@ __device__ void order_by_count(const int32_t* __restrict__ cnt, int n, int32_t* 
   long long total = 0;
 #pragma unroll
   for (int i = 0; i < W; ++i) total += red[i];
-  // Item `it` is long when cnt * n > 2 * total.
-  auto is_long = [&](int it) { return (long long)max(__ldg(cnt + it), 0) * n > 2 * total; };
+  // Item `it` is long when work * n > 2 * total.
+  auto is_long = [&](int it) { return (long long)work(it) * n > 2 * total; };
   int nl = 0;
   for (int it = lo; it < hi; ++it) nl += is_long(it) ? 1 : 0;
-  // Exclusive scan of the per-thread long counts.
   int incl = nl;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -102,25 +107,36 @@ __device__ void order_by_count(const int32_t* __restrict__ cnt, int n, int32_t* 
 }
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
-// CTAs [0, ndelta) compute D; the two CTAs after them build the launch orders
-// of the kv-blocks and of the q-blocks while the rest of the grid streams O
-// and dO.
+// The first two CTAs build the launch orders (key tiles by the summed length
+// of their column lists, q-blocks by row count) while the others stream O and
+// dO.  `kv_per_tile` is 2 when a key tile is a pair of 64-key kv-blocks.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, long long rows,
-    float* __restrict__ delta, unsigned ndelta, const int32_t* __restrict__ col_cnt, int ncol,
-    int32_t* __restrict__ col_order, const int32_t* __restrict__ row_cnt, int nrow,
-    int32_t* __restrict__ row_order) {
-  if (blockIdx.x >= ndelta) {
-    if (blockIdx.x == ndelta)
-      order_by_count<256>(col_cnt, ncol, col_order);
-    else
-      order_by_count<256>(row_cnt, nrow, row_order);
+    float* __restrict__ delta, const int32_t* __restrict__ col_cnt, int BH, int Mk, int Mt,
+    int kv_per_tile, int32_t* __restrict__ tile_order, const int32_t* __restrict__ row_cnt,
+    int nrow, int32_t* __restrict__ row_order) {
+  if (blockIdx.x < 2) {
+    if (blockIdx.x == 0) {
+      auto work = [&](int it) -> long long {
+        const int bh = it / Mt, jt = it % Mt;
+        long long w = 0;
+        for (int e = 0; e < kv_per_tile; ++e) {
+          const int j = jt * kv_per_tile + e;
+          if (j < Mk) w += max(__ldg(col_cnt + (long long)bh * Mk + j), 0);
+        }
+        return w;
+      };
+      order_by_work<256>(BH * Mt, work, tile_order);
+    } else {
+      auto work = [&](int it) -> long long { return max(__ldg(row_cnt + it), 0); };
+      order_by_work<256>(nrow, work, row_order);
+    }
     return;
   }
   constexpr int CH = D / 8;        // 16-byte chunks per row
   constexpr int RPB = 256 / CH;    // rows per block pass
-  const long long r = (long long)blockIdx.x * RPB + threadIdx.x / CH;
+  const long long r = (long long)(blockIdx.x - 2) * RPB + threadIdx.x / CH;
   const int c = threadIdx.x % CH;
   float s = 0.f;
   if (r < rows) {
@@ -141,374 +157,6 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(
   if (c == 0 && r < rows) delta[r] = s;
 }
 
-// Writes 32 bf16 values (half of a 128-byte row: 16-byte chunks 4h .. 4h+3)
-// into a 128-byte-swizzled tile.
-__device__ __forceinline__ void store_half_row_sw128(uint8_t* tile, int row, int half,
-                                                     const uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    uint4 v;
-    v.x = pk[4 * ch + 0];
-    v.y = pk[4 * ch + 1];
-    v.z = pk[4 * ch + 2];
-    v.w = pk[4 * ch + 3];
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, (half * 4 + ch) * 16)) = v;
-  }
-}
-
-// Warp roles of both gradient kernels (352 threads): warps 0-7 compute, with
-// query row (or feature) 32*(w % 4) + lane = TMEM lane and score columns
-// 32*(w / 4) .. +31 (P comes from the saved LSE, so a row needs no exchange
-// between its two warps); warp 8 TMA producer; warp 9 issues the S and dP
-// MMAs; warp 10 issues the gradient MMAs.  Two issuers let the MMAs of
-// neighbouring tiles overlap.
-constexpr int kGradThreads = 352;
-constexpr int kComputeWarps = 8;
-constexpr int kGProducer = 8;
-constexpr int kGIssueA = 9;
-constexpr int kGIssueB = 10;
-
-// ---------------------------------------------------------------- dK, dV
-template <int D>
-struct DkdvCfg {
-  static constexpr int NST = 2;
-  static constexpr int KCH = D / 64;
-  static constexpr uint32_t kKV = kBN * D * 2;  // one K or V tile
-  static constexpr uint32_t kQ = kBM * D * 2;   // one Q or dO tile
-  static constexpr uint32_t kP = kBM * kBN * 2;
-  static constexpr uint32_t off_k = 0;
-  static constexpr uint32_t off_v = off_k + kKV;
-  static constexpr uint32_t off_q = off_v + kKV;                 // NST stages of Q
-  static constexpr uint32_t off_do = off_q + NST * kQ;           // NST stages of dO
-  static constexpr uint32_t off_p = off_do + NST * kQ;           // 2 buffers
-  static constexpr uint32_t off_ds = off_p + 2 * kP;             // 2 buffers
-  static constexpr uint32_t off_bar = off_ds + 2 * kP;
-  static constexpr int B_KV = 0;
-  static constexpr int B_QF = 1;
-  static constexpr int B_QE = B_QF + NST;
-  static constexpr int B_SF = B_QE + NST;  // 2
-  static constexpr int B_PSF = B_SF + 2;   // 2, count 256
-  static constexpr int B_PSE = B_PSF + 2;  // 2
-  static constexpr int B_DONE = B_PSE + 2; // count 2
-  static constexpr int NBAR = B_DONE + 1;
-  static constexpr uint32_t off_slot = off_bar + NBAR * 8;
-  static constexpr uint32_t bytes = off_slot + 16;
-  static constexpr uint32_t smem_alloc = bytes + 1024;
-  static constexpr uint32_t tmem_cols = 512;  // S/dP x2 [0,256), dV^T [256,320), dK^T [320,384)
-  static constexpr uint32_t col_dv = 256;
-  static constexpr uint32_t col_dk = 320;
-};
-
-template <int D>
-__global__ void __launch_bounds__(kGradThreads, 1)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const float* __restrict__ lse, const float* __restrict__ delta,
-                    const int32_t* __restrict__ col_idx, const int32_t* __restrict__ col_cnt,
-                    const int32_t* __restrict__ col_order, int N, int Mq, int Mk, float scale,
-                    float scale_log2, __nv_bfloat16* __restrict__ dk,
-                    __nv_bfloat16* __restrict__ dv, int32_t* __restrict__ status) {
-  using C = DkdvCfg<D>;
-  // The dQ kernel (independent of this one) may start on SMs this grid's
-  // last CTAs leave idle.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  const uint32_t s0 = smem_u32(sm);
-  auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
-  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = min(max(__ldg(col_order + blockIdx.x), 0), static_cast<int>(gridDim.x) - 1);
-  const int bh = item / Mk;
-  const int j = item % Mk;
-  const long long col_id = (long long)bh * Mk + j;
-  const int n = min(max(__ldg(col_cnt + col_id), 0), Mq);
-  const int32_t* list = col_idx + col_id * Mq;
-  const int kv_valid = min(kBN, N - j * kBN);
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i) {
-      uint32_t cnt = 1;
-      if (i == C::B_PSF || i == C::B_PSF + 1) cnt = 32 * kComputeWarps;
-      if (i == C::B_DONE) cnt = 2;
-      mbar_init(bar(i), cnt);
-    }
-    fence_barrier_init();
-  }
-  if (warp == kGIssueA) {
-    tmem_alloc(smem_u32(slot), C::tmem_cols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *slot;
-
-  if (warp == kGProducer) {
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::kKV);
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_3d(s0 + C::off_k + c * kBN * 128, &tmK, bar(C::B_KV), c * 64, j * kBN, bh);
-        tma_load_3d(s0 + C::off_v + c * kBN * 128, &tmV, bar(C::B_KV), c * 64, j * kBN, bh);
-      }
-      int issued = 0;
-      for (int t = 0; t < n; ++t) {
-        const int s = t % C::NST;
-        if (t >= C::NST && !mbar_wait(bar(C::B_QE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
-          report_error(status, SPARGE_ERR_TIMEOUT);
-          break;
-        }
-        const int i = min(max(__ldg(list + t), 0), Mq - 1);
-        mbar_arrive_expect_tx(bar(C::B_QF + s), 2 * C::kQ);
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_3d(s0 + C::off_q + s * C::kQ + c * kBM * 128, &tmQ, bar(C::B_QF + s), c * 64,
-                      i * kBM, bh);
-          tma_load_3d(s0 + C::off_do + s * C::kQ + c * kBM * 128, &tmDO, bar(C::B_QF + s), c * 64,
-                      i * kBM, bh);
-        }
-        issued = t + 1;
-      }
-      for (int t = max(0, issued - C::NST); t < issued; ++t)
-        mbar_wait(bar(C::B_QF + t % C::NST), (t / C::NST) & 1, kWaitTimeoutNs);
-    }
-  } else if (warp == kGIssueA) {
-    // S_t = Q_t K^T and dP_t = dO_t V^T (M = 128 query rows, N = 64 keys).
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-      const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(s0 + C::off_v, 16, 1024);
-      bool ok = mbar_wait(bar(C::B_KV), 0, kWaitTimeoutNs);
-      for (int t = 0; ok && t < n; ++t) {
-        const int s = t % C::NST;
-        // TMEM buffer t & 1 was read by the compute warps of tile t - 2 before
-        // they filled P/dS(t - 2).
-        if (!mbar_wait(bar(C::B_QF + s), (t / C::NST) & 1, kWaitTimeoutNs) ||
-            (t >= 2 && !mbar_wait(bar(C::B_PSF + (t & 1)), ((t - 2) >> 1) & 1, kWaitTimeoutNs))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t dq = sdesc_sw128(s0 + C::off_q + s * C::kQ, 16, 1024);
-        const uint64_t ddo = sdesc_sw128(s0 + C::off_do + s * C::kQ, 16, 1024);
-        const uint32_t dS = tmem + (t & 1) * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16(dS, sdesc_add(dq, ko), sdesc_add(dk0, kko), idS, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16(dS + 64, sdesc_add(ddo, ko), sdesc_add(dv0, kko), idS, kk > 0);
-        }
-        tc_commit(bar(C::B_SF + (t & 1)));
-      }
-      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      tc_commit(bar(C::B_DONE));
-      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
-    }
-  } else if (warp == kGIssueB) {
-    // dV^T += dO_u^T P_u and dK^T += Q_u^T dS_u (M = d, N = 64 keys, K = 16
-    // query rows per step; A and B read MN-major).
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t idG = idesc_bf16(kBM, kBN, true, true);
-      bool ok = true;
-      for (int u = 0; ok && u < n; ++u) {
-        const int su = u % C::NST;
-        const int pb = u & 1;
-        if (!mbar_wait(bar(C::B_PSF + pb), (u >> 1) & 1, kWaitTimeoutNs)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t dq = sdesc_sw128(s0 + C::off_q + su * C::kQ, kBM * 128, 1024);
-        const uint64_t ddo = sdesc_sw128(s0 + C::off_do + su * C::kQ, kBM * 128, 1024);
-        const uint64_t dpb = sdesc_sw128(s0 + C::off_p + pb * C::kP, kBM * 128, 1024);
-        const uint64_t dsb = sdesc_sw128(s0 + C::off_ds + pb * C::kP, kBM * 128, 1024);
-#pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)
-          tc_mma_bf16(tmem + C::col_dv, sdesc_add(ddo, kk * 2048), sdesc_add(dpb, kk * 2048), idG,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)
-          tc_mma_bf16(tmem + C::col_dk, sdesc_add(dq, kk * 2048), sdesc_add(dsb, kk * 2048), idG,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-        // S/dP(u) completed before P/dS(u) were written, so the Q/dO stage is
-        // free once these MMAs complete.
-        tc_commit(bar(C::B_QE + su));
-        tc_commit(bar(C::B_PSE + pb));
-      }
-      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      tc_commit(bar(C::B_DONE));
-      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
-    }
-  } else {
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;
-    const int c0 = half * 32;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    bool ok = true;
-    // Two-deep prefetch: the q-block index of tile t+2 and the LSE / D of
-    // tile t+1 are loaded while tile t is computed.
-    const float* lse_h = lse + (long long)bh * N;
-    const float* del_h = delta + (long long)bh * N;
-    auto row_of = [&](int qi) { return qi * kBM + r; };
-    int i_n1 = n > 0 ? min(max(__ldg(list), 0), Mq - 1) : 0;
-    int i_n2 = n > 1 ? min(max(__ldg(list + 1), 0), Mq - 1) : 0;
-    float lse_n = 0.f, del_n = 0.f;
-    if (n > 0 && row_of(i_n1) < N) {
-      lse_n = __ldg(lse_h + row_of(i_n1));
-      del_n = __ldg(del_h + row_of(i_n1));
-    }
-    for (int t = 0; t < n; ++t) {
-      const bool rv = row_of(i_n1) < N;
-      const float lse2 = rv ? lse_n * kLog2e : 0.f;
-      const float drow = rv ? del_n : 0.f;
-      i_n1 = i_n2;
-      if (t + 1 < n && row_of(i_n1) < N) {
-        lse_n = __ldg(lse_h + row_of(i_n1));
-        del_n = __ldg(del_h + row_of(i_n1));
-      }
-      if (t + 2 < n) i_n2 = min(max(__ldg(list + t + 2), 0), Mq - 1);
-      if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t pk[16], dk_[16];
-      {
-        float s[32], dp[32];
-        tmem_ld32(lane_base + (t & 1) * 128 + c0, s);
-        tmem_ld32(lane_base + (t & 1) * 128 + 64 + c0, dp);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float p0 = ex2_approx(fmaf(s[c], scale_log2, -lse2));
-          float p1 = ex2_approx(fmaf(s[c + 1], scale_log2, -lse2));
-          if (!rv || c0 + c >= kv_valid) p0 = 0.f;
-          if (!rv || c0 + c + 1 >= kv_valid) p1 = 0.f;
-          pk[c / 2] = pack_bf16x2(p0, p1);
-          dk_[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
-        }
-      }
-      // Buffer t & 1 is free once the dV/dK MMAs of tile t-2 have completed.
-      if (t >= 2 && !warp_wait(bar(C::B_PSE + (t & 1)), ((t - 2) >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      store_half_row_sw128(sm + C::off_p + (t & 1) * C::kP, r, half, pk);
-      store_half_row_sw128(sm + C::off_ds + (t & 1) * C::kP, r, half, dk_);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_PSF + (t & 1)));
-    }
-    if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-    // Epilogue: lane r holds feature r of dV^T / dK^T; this warp writes the 32
-    // keys c0 .. c0+31 of it.
-    bool have = ok && n > 0;
-    if (have) {
-      have = warp_wait(bar(C::B_PSE + ((n - 1) & 1)), ((n - 1) >> 1) & 1);
-      if (!have) report_error(status, SPARGE_ERR_TIMEOUT);
-    }
-    tc_fence_after();
-    const long long base = ((long long)bh * N + (long long)j * kBN) * D + r;
-#pragma unroll 1
-    for (int cc = c0; cc < c0 + 32; cc += 16) {
-      uint32_t rv_[16], rk_[16];
-      if (have) {
-        SPARGE_TMEM_LD_X16(lane_base + C::col_dv + cc, rv_);
-        SPARGE_TMEM_LD_X16(lane_base + C::col_dk + cc, rk_);
-        SPARGE_TMEM_WAIT_LD16(rv_);
-        SPARGE_TMEM_WAIT_LD16(rk_);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) rv_[c] = rk_[c] = 0u;
-      }
-      if (r < D) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          if (cc + c < kv_valid) {
-            __stcs(dv + base + (long long)(cc + c) * D, __float2bfloat16_rn(__uint_as_float(rv_[c])));
-            __stcs(dk + base + (long long)(cc + c) * D,
-                   __float2bfloat16_rn(__uint_as_float(rk_[c]) * scale));
-          }
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kGIssueA) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::tmem_cols);
-  }
-}
-
-// ---------------------------------------------------------------- dQ
-template <int D>
-struct DqCfg {
-  static constexpr int KCH = D / 64;
-  static constexpr uint32_t kKV = kBN * D * 2;
-  static constexpr uint32_t kQ = kBM * D * 2;
-  static constexpr int NST = 4;
-  static constexpr uint32_t off_q = 0;
-  static constexpr uint32_t off_do = off_q + kQ;
-  static constexpr uint32_t off_k = off_do + kQ;
-  static constexpr uint32_t off_v = off_k + NST * kKV;
-  static constexpr uint32_t off_bar = off_v + NST * kKV;
-  static constexpr int B_Q = 0;
-  static constexpr int B_QT = 1;            // Q, dO copied into TMEM (count 256)
-  static constexpr int B_KF = 2;
-  static constexpr int B_VF = B_KF + NST;
-  static constexpr int B_KE = B_VF + NST;   // K slot free (dQ of its tile done)
-  static constexpr int B_VE = B_KE + NST;   // V slot free (dP of its tile done)
-  static constexpr int B_SF = B_VE + NST;   // 2
-  static constexpr int B_DSF = B_SF + 2;    // 2, count 256 (dS written)
-  static constexpr int B_DSE = B_DSF + 2;   // 2 (dQ of the tile done: TMEM tile free)
-  static constexpr int B_DONE = B_DSE + 2;  // count 2
-  static constexpr int NBAR = B_DONE + 1;
-  static constexpr uint32_t off_slot = off_bar + NBAR * 8;
-  static constexpr uint32_t bytes = off_slot + 16;
-  static constexpr uint32_t smem_alloc = bytes + 1024;
-  // TMEM: S/dP x2 [0,256) (S_b at 128b, dP_b at 128b + 64), dQ [256, 256+D),
-  // Q and dO as MMA A operands (bf16 pairs, D/2 columns each) after it.  dS_t
-  // (bf16 pairs, 32 columns) goes over columns 16..47 of S_t's tile: the half
-  // of a row that read S columns 0..31 writes 16..31, the other 32..47, so no
-  // warp overwrites columns another warp has still to read.  Q and dO in TMEM
-  // keep their operand reads (reused by every tile) out of shared memory.
-  static constexpr uint32_t tmem_cols = 512;
-  static constexpr uint32_t col_dq = 256;
-  static constexpr uint32_t col_q = 256 + D;
-  static constexpr uint32_t col_do = col_q + D / 2;
-  static constexpr uint32_t col_ds = 16;
-};
-
-// Copies this thread's half row of a 128-byte-swizzled bf16 tile (rows of D
-// values, 64-column chunks 128 * kBM bytes apart) into TMEM lane `lane_addr`
-// as bf16 pairs: D/4 columns starting at column half * D/4.
-template <int D>
-__device__ __forceinline__ void tile_half_row_to_tmem(const uint8_t* tile, int row, int half,
-                                                      uint32_t lane_addr) {
-  constexpr int W = D / 4;  // 32-bit columns per half row
-  uint32_t v[W];
-#pragma unroll
-  for (int q4 = 0; q4 < W / 4; ++q4) {
-    const int byte = half * (D / 2) * 2 + q4 * 16;  // byte offset within the row
-    const uint4 u = *reinterpret_cast<const uint4*>(tile + (byte / 128) * (kBM * 128) +
-                                                    sw128_offset(row, byte % 128));
-    v[4 * q4 + 0] = u.x;
-    v[4 * q4 + 1] = u.y;
-    v[4 * q4 + 2] = u.z;
-    v[4 * q4 + 3] = u.w;
-  }
-#pragma unroll
-  for (int c = 0; c < W; c += 16) SPARGE_TMEM_ST_X16(lane_addr + half * W + c, (v + c));
-}
-
 // tcgen05.mma kind::f16 with the A operand in tensor memory (M lanes, K/2
 // 32-bit columns holding bf16 pairs, element 2c in the low half of column c).
 __device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
@@ -521,14 +169,529 @@ __device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// Loads 32 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32u(uint32_t addr, uint32_t (&a)[16], uint32_t (&b)[16]) {
+  SPARGE_TMEM_LD_X16(addr, a);
+  SPARGE_TMEM_LD_X16(addr + 16, b);
+  SPARGE_TMEM_WAIT_LD16(a);
+  SPARGE_TMEM_WAIT_LD16(b);
+}
+
+// Warp roles of the gradient kernels: CW compute warps (CW / 4 per TMEM lane
+// quarter), then a TMA producer warp, a warp issuing the S and dP MMAs and a
+// warp issuing the gradient MMAs.  The dQ kernel runs sixteen compute warps
+// (four per SM sub-partition, to hide the tensor-memory and exponential
+// latencies of its short per-thread rows); the dK/dV kernel eight, whose
+// threads carry 32 columns per query half (measured: sixteen were slower).
+template <int CW>
+struct Roles {
+  static constexpr int kCompute = CW;
+  static constexpr int kThreads = (CW + 3) * 32;
+  static constexpr int kProducer = CW;
+  static constexpr int kIssueA = CW + 1;
+  static constexpr int kIssueB = CW + 2;
+};
+constexpr int kDkdvWarps = 8;
+constexpr int kDqWarps = 16;
+
+// ---------------------------------------------------------------- dK, dV
 template <int D>
-__global__ void __launch_bounds__(kGradThreads, 1)
+struct DkdvCfg {
+  // Q and dO arrive per 64-query half of a q-block: a slot holds Q_h and dO_h
+  // (64 rows each) and is released once the gradient MMAs of that half are done.
+  static constexpr int NSLOT = D == 128 ? 4 : 8;
+  static constexpr uint32_t kKP = kPair * D * 2;     // K (or V) of the 128 keys
+  static constexpr uint32_t kQh = 64 * D * 2;        // one Q (or dO) half tile
+  static constexpr uint32_t kChunkK = kPair * 128;   // 64-column chunk of the key tile
+  static constexpr uint32_t kChunkH = 64 * 128;      // 64-column chunk of a half tile
+  static constexpr uint32_t off_k = 0;
+  static constexpr uint32_t off_v = off_k + kKP;
+  static constexpr uint32_t off_q = off_v + kKP;               // NSLOT Q halves
+  static constexpr uint32_t off_do = off_q + NSLOT * kQh;      // NSLOT dO halves
+  static constexpr uint32_t off_row = off_do + NSLOT * kQh;    // NSLOT x {lse*log2e [64], D [64]}
+  static constexpr uint32_t off_info = off_row + NSLOT * 2 * 64 * 4;  // NSLOT x int32
+  static constexpr uint32_t off_bar = off_info + 64;
+  static constexpr int B_KV = 0;
+  static constexpr int B_QF = 1;              // NSLOT, count 32 (producer lanes) + tx
+  static constexpr int B_QE = B_QF + NSLOT;   // NSLOT: the half's gradient MMAs done
+  // Per query half h, S^T and dP^T are tracked separately, so that P^T and
+  // dV of a half proceed while dP^T and dS^T of it are still in flight.
+  static constexpr int B_SSF = B_QE + NSLOT;  // 2: S^T_h in TMEM
+  static constexpr int B_DPF = B_SSF + 2;     // 2: dP^T_h in TMEM
+  static constexpr int B_PPF = B_DPF + 2;     // 2, count 256: P^T_h written
+  static constexpr int B_DSF = B_PPF + 2;     // 2, count 256: dS^T_h written
+  static constexpr int B_RVF = B_DSF + 2;     // 2: dV MMAs of half h done (S^T_h region free)
+  static constexpr int B_RKF = B_RVF + 2;     // 2: dK MMAs of half h done (dP^T_h region free)
+  static constexpr int B_DONE = B_RKF + 2;    // count 2
+  static constexpr int NBAR = B_DONE + 1;
+  static constexpr uint32_t off_slot = off_bar + NBAR * 8;
+  static constexpr uint32_t bytes = off_slot + 16;
+  static constexpr uint32_t smem_alloc = bytes + 1024;
+  // TMEM: half h of the queries uses columns [128h, 128h + 128): S^T_h at
+  // +0 (64 fp32 columns) and dP^T_h at +64.  P^T_h is written over S^T_h as
+  // bf16 pairs: the compute group holding queries NC*g .. NC*g + NC - 1 (NC
+  // = 32 with eight compute warps) writes them to columns NC*g .. NC*g +
+  // NC/2 - 1, over columns it had read; dS^T_h likewise over dP^T_h.  dV at
+  // 256, dK at 256 + 128.
+  static constexpr uint32_t tmem_cols = 512;
+  static constexpr uint32_t col_dv = 256;
+  static constexpr uint32_t col_dk = 384;
+};
+
+// One CTA per key tile: 128 keys = the 64-key kv-blocks j0 = 2 * jt and
+// j1 = 2 * jt + 1 (kv_per_tile = 2), or the one 128-key block jt
+// (kv_per_tile = 1; then both 64-row halves belong to it).
+template <int D>
+__global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const float* __restrict__ lse, const float* __restrict__ delta,
+                    const int32_t* __restrict__ col_idx, const int32_t* __restrict__ col_cnt,
+                    const int32_t* __restrict__ tile_order, int N, int Mq, int Mk, int Mt,
+                    int kv_per_tile, float scale, float scale_log2,
+                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                    int32_t* __restrict__ status) {
+  using C = DkdvCfg<D>;
+  // The dQ kernel (independent of this one) may start on SMs this grid's
+  // last CTAs leave idle.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t s0 = smem_u32(sm);
+  auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
+  int32_t* info = reinterpret_cast<int32_t*>(sm + C::off_info);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = min(max(__ldg(tile_order + blockIdx.x), 0), static_cast<int>(gridDim.x) - 1);
+  const int bh = item / Mt;
+  const int jt = item % Mt;
+  const int key0 = jt * kPair;  // first key token of the tile
+
+  // The two column lists (one list, taken for both halves, for a 128-key block).
+  const bool paired = kv_per_tile == 2;
+  const int ja = paired ? 2 * jt : jt;
+  const int jb = paired ? 2 * jt + 1 : jt;
+  const int32_t* list0 = col_idx + ((long long)bh * Mk + ja) * Mq;
+  const int32_t* list1 = col_idx + ((long long)bh * Mk + min(jb, Mk - 1)) * Mq;
+  const int n0 = min(max(__ldg(col_cnt + (long long)bh * Mk + ja), 0), Mq);
+  const int n1 = (paired && jb < Mk) ? min(max(__ldg(col_cnt + (long long)bh * Mk + jb), 0), Mq) : 0;
+
+  // Length of the union of the two ascending lists: n0 + n1 minus the common
+  // entries, counted by binary search of list0's entries in list1.
+  if (threadIdx.x == 0) slot[1] = 0;
+  __syncthreads();
+  if (paired) {
+    int common = 0;
+    for (int e = threadIdx.x; e < n0; e += Roles<kDkdvWarps>::kThreads) {
+      const int x = __ldg(list0 + e);
+      int lo = 0, hi = n1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(list1 + mid) < x) lo = mid + 1; else hi = mid;
+      }
+      common += (lo < n1 && __ldg(list1 + lo) == x) ? 1 : 0;
+    }
+    if (common) atomicAdd(reinterpret_cast<int*>(slot + 1), common);
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i >= C::B_QF && i < C::B_QF + C::NSLOT) cnt = 32;
+      if (i >= C::B_PPF && i < C::B_PPF + 4) cnt = 32 * Roles<kDkdvWarps>::kCompute;  // PPF, DSF
+      if (i == C::B_DONE) cnt = 2;
+      mbar_init(bar(i), cnt);
+    }
+    fence_barrier_init();
+  }
+  if (warp == Roles<kDkdvWarps>::kIssueA) {
+    tmem_alloc(smem_u32(slot), C::tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = slot[0];
+  const int n = paired ? n0 + n1 - static_cast<int>(slot[1]) : n0;
+
+  if (warp == Roles<kDkdvWarps>::kProducer) {
+    // ---------------------------------------------------------- producer
+    if (n > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::kKP);
+        for (int c = 0; c < D / 64; ++c) {
+          const uint32_t o = c * C::kChunkK;
+          tma_load_3d(s0 + C::off_k + o, &tmK, bar(C::B_KV), c * 64, key0, bh);
+          tma_load_3d(s0 + C::off_k + o + kBN * 128, &tmK, bar(C::B_KV), c * 64, key0 + kBN, bh);
+          tma_load_3d(s0 + C::off_v + o, &tmV, bar(C::B_KV), c * 64, key0, bh);
+          tma_load_3d(s0 + C::off_v + o + kBN * 128, &tmV, bar(C::B_KV), c * 64, key0 + kBN, bh);
+        }
+      }
+      const float* lse_h = lse + (long long)bh * N;
+      const float* del_h = delta + (long long)bh * N;
+      int a = 0, b = 0, issued = 0;
+      bool ok = true;
+      for (int t = 0; ok && t < n; ++t) {
+        // Next entry of the union (every lane walks the lists identically).
+        const int x0 = a < n0 ? min(max(__ldg(list0 + a), 0), Mq - 1) : Mq;
+        const int x1 = b < n1 ? min(max(__ldg(list1 + b), 0), Mq - 1) : Mq;
+        const int i = min(x0, x1);
+        int flags = paired ? ((x0 == i ? 1 : 0) | (x1 == i ? 2 : 0)) : 3;
+        if (x0 == i) ++a;
+        if (x1 == i) ++b;
+        if (i >= Mq) flags = 0;  // lists shorter than their counts claim: no work
+        const int ic = min(i, Mq - 1);
+        for (int h = 0; h < 2; ++h) {
+          const int k = 2 * t + h, sl = k % C::NSLOT;
+          if (k >= C::NSLOT &&
+              !mbar_wait(bar(C::B_QE + sl), ((k / C::NSLOT) - 1) & 1, kWaitTimeoutNs))
+            ok = false;
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            report_error(status, SPARGE_ERR_TIMEOUT);
+            break;
+          }
+          const int row0 = ic * kBM + h * 64;
+          if (lane == 0) {
+            mbar_expect_tx(bar(C::B_QF + sl), 2 * C::kQh);
+            for (int c = 0; c < D / 64; ++c) {
+              tma_load_3d(s0 + C::off_q + sl * C::kQh + c * C::kChunkH, &tmQ, bar(C::B_QF + sl),
+                          c * 64, row0, bh);
+              tma_load_3d(s0 + C::off_do + sl * C::kQh + c * C::kChunkH, &tmDO,
+                          bar(C::B_QF + sl), c * 64, row0, bh);
+            }
+            info[sl] = ic | (flags << 24);
+          }
+          // lse * log2(e) and D of the half's 64 tokens (queries past N get
+          // +inf and 0, so that their P and dS are 0).
+          float2 l2, d2;
+          const int tok = row0 + lane * 2;
+          l2.x = tok < N ? __ldg(lse_h + tok) * kLog2e : INFINITY;
+          l2.y = tok + 1 < N ? __ldg(lse_h + tok + 1) * kLog2e : INFINITY;
+          d2.x = tok < N ? __ldg(del_h + tok) : 0.f;
+          d2.y = tok + 1 < N ? __ldg(del_h + tok + 1) : 0.f;
+          float* rowv = reinterpret_cast<float*>(sm + C::off_row + sl * (2 * 64 * 4));
+          reinterpret_cast<float2*>(rowv)[lane] = l2;
+          reinterpret_cast<float2*>(rowv + 64)[lane] = d2;
+          mbar_arrive(bar(C::B_QF + sl));
+          issued = k + 1;
+        }
+      }
+      // Let the last loads land before the CTA can exit.
+      if (lane == 0) {
+        mbar_wait(bar(C::B_KV), 0, kWaitTimeoutNs);
+        for (int k = max(0, issued - C::NSLOT); k < issued; ++k)
+          mbar_wait(bar(C::B_QF + k % C::NSLOT), (k / C::NSLOT) & 1, kWaitTimeoutNs);
+      }
+    }
+  } else if (warp == Roles<kDkdvWarps>::kIssueA) {
+    // ---------------------------------------------------------- S^T, dP^T
+    // S^T_h = K Q_h^T and dP^T_h = V dO_h^T (M = 128 keys, N = 64 queries of
+    // half h, K = d).
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idS = idesc_bf16(kPair, 64, false, false);
+      const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(s0 + C::off_v, 16, 1024);
+      bool ok = mbar_wait(bar(C::B_KV), 0, kWaitTimeoutNs);
+      for (int t = 0; ok && t < n; ++t) {
+        for (int h = 0; h < 2; ++h) {
+          const int k = 2 * t + h, sl = k % C::NSLOT;
+          // S^T_h's columns hold P^T_h of entry t - 1 until its dV MMAs are
+          // done, dP^T_h's hold dS^T_h until its dK MMAs are.
+          if (!mbar_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1, kWaitTimeoutNs) ||
+              (t >= 1 && !mbar_wait(bar(C::B_RVF + h), (t - 1) & 1, kWaitTimeoutNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, 16, 1024);
+          const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, 16, 1024);
+          const uint32_t dS = tmem + h * 128;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+            const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
+            tc_mma_bf16(dS, sdesc_add(dk0, ka), sdesc_add(dq, kb), idS, kk > 0);
+          }
+          tc_commit(bar(C::B_SSF + h));
+          if (t >= 1 && !mbar_wait(bar(C::B_RKF + h), (t - 1) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+            const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
+            tc_mma_bf16(dS + 64, sdesc_add(dv0, ka), sdesc_add(ddo, kb), idS, kk > 0);
+          }
+          tc_commit(bar(C::B_DPF + h));
+        }
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+      tc_commit(bar(C::B_DONE));
+      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+    }
+  } else if (warp == Roles<kDkdvWarps>::kIssueB) {
+    // ---------------------------------------------------------- dV, dK
+    // dV += P^T_h dO_h and dK += dS^T_h Q_h (M = 128 keys, N = d, K = the 64
+    // queries of half h); A from TMEM, B = dO_h / Q_h read MN-major.
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idG = idesc_bf16(kPair, D, false, true);
+      bool ok = true;
+      for (int t = 0; ok && t < n; ++t) {
+        for (int h = 0; h < 2; ++h) {
+          const int sl = (2 * t + h) % C::NSLOT;
+          const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, C::kChunkH, 1024);
+          const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, C::kChunkH, 1024);
+          const uint32_t ap = tmem + h * 128;
+          // Queries 16kk .. 16kk + 15 of the half: the TMEM columns where the
+          // compute warp group holding them wrote their bf16 pairs.
+          constexpr int NC = 64 / (Roles<kDkdvWarps>::kCompute / 4);
+          if (!mbar_wait(bar(C::B_PPF + h), t & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16_ta(tmem + C::col_dv, ap + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
+                           sdesc_add(ddo, kk * 2048), idG,
+                           (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(C::B_RVF + h));
+          if (!mbar_wait(bar(C::B_DSF + h), t & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16_ta(tmem + C::col_dk, ap + 64 + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
+                           sdesc_add(dq, kk * 2048), idG,
+                           (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(C::B_RKF + h));
+          tc_commit(bar(C::B_QE + sl));
+        }
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+      tc_commit(bar(C::B_DONE));
+      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+    }
+  } else {
+    // ---------------------------------------------------------- compute
+    // Thread = key row r (TMEM lane).  All compute warps take half 0 of an
+    // entry, then half 1; within a half, warp group g = warp / 4 takes the NC
+    // queries NC*g .. NC*g + NC - 1.
+    constexpr int NC = 64 / (Roles<kDkdvWarps>::kCompute / 4);
+    const int quarter = warp & 3, cg = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool key_in = key0 + r < N;
+    const int flag_bit = r < kBN ? 1 : 2;  // warp-uniform (quarters 0-1 vs 2-3)
+    bool ok = true;
+    for (int t = 0; ok && t < n; ++t) {
+      for (int h = 0; h < 2; ++h) {
+        const int k = 2 * t + h, sl = k % C::NSLOT;
+        if (!warp_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1) ||
+            !warp_wait(bar(C::B_SSF + h), t & 1)) {
+          ok = false;
+          break;
+        }
+        const int flags = info[sl] >> 24;
+        const bool live = (flags & flag_bit) != 0;  // warp-uniform
+        const float* rowv = reinterpret_cast<const float*>(sm + C::off_row + sl * (2 * 64 * 4));
+        tc_fence_after();
+        const uint32_t sa = lane_base + h * 128 + NC * cg;
+        // P^T first (from S^T alone); it is the A operand of dV.
+        float p[NC];
+        uint32_t pk[NC / 2];
+        if (live) {
+          uint32_t sr[NC / 16][16];
+#pragma unroll
+          for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 16 * c, sr[c]);
+#pragma unroll
+          for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(sr[c]);
+          const float4* l4 = reinterpret_cast<const float4*>(rowv + NC * cg);
+#pragma unroll
+          for (int g = 0; g < NC / 4; ++g) {
+            const float4 lv = l4[g];
+            const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = g * 4 + e;
+              p[col] = ex2_approx(fmaf(__uint_as_float(sr[col / 16][col % 16]), scale_log2, -lq[e]));
+            }
+          }
+          if (!key_in) {
+#pragma unroll
+            for (int e = 0; e < NC; ++e) p[e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < NC / 2; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < NC; ++e) p[e] = 0.f;
+#pragma unroll
+          for (int e = 0; e < NC / 2; ++e) pk[e] = 0u;
+        }
+        // P^T over the first NC/2 of the NC S^T columns this thread read.
+        if constexpr (NC == 32) {
+          SPARGE_TMEM_ST_X16(sa, pk);
+        } else {
+          SPARGE_TMEM_ST_X8(sa, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PPF + h));
+        // dS^T = P^T * (dP^T - D).
+        if (!warp_wait(bar(C::B_DPF + h), t & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (live) {
+          uint32_t dr[NC / 16][16];
+#pragma unroll
+          for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 64 + 16 * c, dr[c]);
+#pragma unroll
+          for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(dr[c]);
+          const float4* d4 = reinterpret_cast<const float4*>(rowv + 64 + NC * cg);
+#pragma unroll
+          for (int g = 0; g < NC / 4; ++g) {
+            const float4 dv4 = d4[g];
+            const float dq4[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+            float ds[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = g * 4 + e;
+              ds[e] = p[col] * (__uint_as_float(dr[col / 16][col % 16]) - dq4[e]);
+            }
+            pk[g * 2 + 0] = pack_bf16x2(ds[0], ds[1]);
+            pk[g * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+          }
+        }
+        if constexpr (NC == 32) {
+          SPARGE_TMEM_ST_X16(sa + 64, pk);
+        } else {
+          SPARGE_TMEM_ST_X8(sa + 64, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DSF + h));
+      }
+    }
+    if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+    // Epilogue: lane r holds key r of dV and dK; warp group cg writes its
+    // share of the features.
+    bool have = ok && n > 0;
+    if (have) {
+      have = warp_wait(bar(C::B_RKF + 0), (n - 1) & 1) && warp_wait(bar(C::B_RKF + 1), (n - 1) & 1);
+      if (!have) report_error(status, SPARGE_ERR_TIMEOUT);
+    }
+    tc_fence_after();
+    const long long rowoff = ((long long)bh * N + key0 + r) * D;
+#pragma unroll 1
+    constexpr int FPW = D / (Roles<kDkdvWarps>::kCompute / 4);  // features per warp
+    for (int cc = cg * FPW; cc < (cg + 1) * FPW; cc += 16) {
+      uint32_t rv_[16], rk_[16];
+      if (have) {
+        SPARGE_TMEM_LD_X16(lane_base + C::col_dv + cc, rv_);
+        SPARGE_TMEM_LD_X16(lane_base + C::col_dk + cc, rk_);
+        SPARGE_TMEM_WAIT_LD16(rv_);
+        SPARGE_TMEM_WAIT_LD16(rk_);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) rv_[c] = rk_[c] = 0u;
+      }
+      if (key_in) {
+        uint4 v0, v1, k0, k1;
+        v0.x = pack_bf16x2(__uint_as_float(rv_[0]), __uint_as_float(rv_[1]));
+        v0.y = pack_bf16x2(__uint_as_float(rv_[2]), __uint_as_float(rv_[3]));
+        v0.z = pack_bf16x2(__uint_as_float(rv_[4]), __uint_as_float(rv_[5]));
+        v0.w = pack_bf16x2(__uint_as_float(rv_[6]), __uint_as_float(rv_[7]));
+        v1.x = pack_bf16x2(__uint_as_float(rv_[8]), __uint_as_float(rv_[9]));
+        v1.y = pack_bf16x2(__uint_as_float(rv_[10]), __uint_as_float(rv_[11]));
+        v1.z = pack_bf16x2(__uint_as_float(rv_[12]), __uint_as_float(rv_[13]));
+        v1.w = pack_bf16x2(__uint_as_float(rv_[14]), __uint_as_float(rv_[15]));
+        k0.x = pack_bf16x2(__uint_as_float(rk_[0]) * scale, __uint_as_float(rk_[1]) * scale);
+        k0.y = pack_bf16x2(__uint_as_float(rk_[2]) * scale, __uint_as_float(rk_[3]) * scale);
+        k0.z = pack_bf16x2(__uint_as_float(rk_[4]) * scale, __uint_as_float(rk_[5]) * scale);
+        k0.w = pack_bf16x2(__uint_as_float(rk_[6]) * scale, __uint_as_float(rk_[7]) * scale);
+        k1.x = pack_bf16x2(__uint_as_float(rk_[8]) * scale, __uint_as_float(rk_[9]) * scale);
+        k1.y = pack_bf16x2(__uint_as_float(rk_[10]) * scale, __uint_as_float(rk_[11]) * scale);
+        k1.z = pack_bf16x2(__uint_as_float(rk_[12]) * scale, __uint_as_float(rk_[13]) * scale);
+        k1.w = pack_bf16x2(__uint_as_float(rk_[14]) * scale, __uint_as_float(rk_[15]) * scale);
+        __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc), v0);
+        __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc + 8), v1);
+        __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc), k0);
+        __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc + 8), k1);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Roles<kDkdvWarps>::kIssueA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------- dQ
+template <int D>
+struct DqCfg {
+  // K slots outnumber V slots: a K slot is held until dQ of its step, a V
+  // slot only until dP.
+  static constexpr int NSK = D == 128 ? 3 : 6;
+  static constexpr int NSV = D == 128 ? 2 : 4;
+  static constexpr uint32_t kKP = kPair * D * 2;    // K (or V) of 128 keys
+  static constexpr uint32_t kQ = kBM * D * 2;
+  static constexpr uint32_t kChunkK = kPair * 128;
+  static constexpr uint32_t kChunkQ = kBM * 128;
+  static constexpr uint32_t off_q = 0;
+  static constexpr uint32_t off_do = off_q + kQ;
+  static constexpr uint32_t off_k = off_do + kQ;        // NSK slots of K
+  static constexpr uint32_t off_v = off_k + NSK * kKP;  // NSV slots of V
+  static constexpr uint32_t off_bar = off_v + NSV * kKP;
+  static constexpr int B_Q = 0;            // Q, dO landed
+  static constexpr int B_KF = 1;           // NSK: K landed
+  static constexpr int B_VF = B_KF + NSK;  // NSV: V landed
+  static constexpr int B_KE = B_VF + NSV;  // NSK: K slot free (dQ of its step done)
+  static constexpr int B_VE = B_KE + NSK;  // NSV: V slot free (dP of its step done)
+  static constexpr int B_SF = B_VE + NSV;  // 2: S in TMEM buffer b
+  static constexpr int B_SE = B_SF + 2;    // 2: dQ read dS of buffer b (buffer free)
+  static constexpr int B_DSF = B_SE + 2;   // 2, count 256: dS written into buffer b
+  static constexpr int B_DPF = B_DSF + 2;  // dP complete
+  static constexpr int B_DPE = B_DPF + 1;  // dP read by every compute thread (count 256)
+  static constexpr int B_DONE = B_DPE + 1; // count 2
+  static constexpr int NBAR = B_DONE + 1;
+  static constexpr uint32_t off_slot = off_bar + NBAR * 8;
+  static constexpr uint32_t bytes = off_slot + 16;
+  static constexpr uint32_t smem_alloc = bytes + 1024;
+  // TMEM: dQ [0, D), S of step u in buffer u % 2 at 128 + 128 * (u % 2) (128
+  // keys; dS of keys 32g .. 32g + 31 written over its columns 32g .. 32g + 15
+  // as bf16 pairs), dP at 384.
+  static constexpr uint32_t tmem_cols = 512;
+  static constexpr uint32_t col_dq = 0;
+  static constexpr uint32_t col_s = 128;
+  static constexpr uint32_t col_dp = 384;
+};
+
+// One CTA per q-block.  Its list of kept kv-blocks is taken two entries at a
+// time (kv_per_entry = 1: 64-key blocks; the second of an odd count is
+// empty), or one 128-key block per step (kv_per_entry = 2).  Q and dO stay in
+// shared memory as the A operands of S and dP; S is double-buffered in TMEM,
+// so S of the next step is computed while the compute warps work on this one.
+template <int D>
+__global__ void __launch_bounds__(Roles<kDqWarps>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const float* __restrict__ lse, const float* __restrict__ delta,
                   const int32_t* __restrict__ row_idx, const int32_t* __restrict__ row_cnt,
-                  const int32_t* __restrict__ row_order, int N, int Mq, int Mk, float scale,
-                  float scale_log2, __nv_bfloat16* __restrict__ dq, int32_t* __restrict__ status) {
+                  const int32_t* __restrict__ row_order, int N, int Mq, int Mk, int kv_per_entry,
+                  float scale, float scale_log2, __nv_bfloat16* __restrict__ dq,
+                  int32_t* __restrict__ status) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -544,17 +707,27 @@ __global__ void __launch_bounds__(kGradThreads, 1)
   const long long row_id = (long long)bh * Mq + qb;
   const int n = min(max(__ldg(row_cnt + row_id), 0), Mk);
   const int32_t* list = row_idx + row_id * Mk;
+  const bool single = kv_per_entry == 1;
+  const int npair = single ? (n + 1) / 2 : n;
+  // First row (in tokens) of the two 64-key halves of step u; -1 = empty half.
+  auto half_row = [&](int u, int half) -> int {
+    if (single) {
+      const int e = 2 * u + half;
+      return e < n ? min(max(__ldg(list + e), 0), Mk - 1) * kBN : -1;
+    }
+    return min(max(__ldg(list + u), 0), Mk - 1) * kPair + half * kBN;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == C::B_DSF || i == C::B_DSF + 1 || i == C::B_QT) cnt = 32 * kComputeWarps;
+      if (i == C::B_DPE || i == C::B_DSF || i == C::B_DSF + 1) cnt = 32 * Roles<kDqWarps>::kCompute;
       if (i == C::B_DONE) cnt = 2;
       mbar_init(bar(i), cnt);
     }
     fence_barrier_init();
   }
-  if (warp == kGIssueA) {
+  if (warp == Roles<kDqWarps>::kIssueA) {
     tmem_alloc(smem_u32(slot), C::tmem_cols);
     tmem_relinquish();
   }
@@ -563,170 +736,200 @@ __global__ void __launch_bounds__(kGradThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *slot;
 
-  if (warp == kGProducer) {
+  if (warp == Roles<kDqWarps>::kProducer) {
+    // ---------------------------------------------------------- producer
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::kQ);
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_3d(s0 + C::off_q + c * kBM * 128, &tmQ, bar(C::B_Q), c * 64, qb * kBM, bh);
-        tma_load_3d(s0 + C::off_do + c * kBM * 128, &tmDO, bar(C::B_Q), c * 64, qb * kBM, bh);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(s0 + C::off_q + c * C::kChunkQ, &tmQ, bar(C::B_Q), c * 64, qb * kBM, bh);
+        tma_load_3d(s0 + C::off_do + c * C::kChunkQ, &tmDO, bar(C::B_Q), c * 64, qb * kBM, bh);
       }
       int issued = 0;
-      for (int t = 0; t < n; ++t) {
-        const int s = t % C::NST;
-        if (t >= C::NST && !mbar_wait(bar(C::B_KE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+      for (int u = 0; u < npair; ++u) {
+        const int sk = u % C::NSK, sv = u % C::NSV;
+        int rw[2];
+        for (int half = 0; half < 2; ++half) {
+          rw[half] = half_row(u, half);
+          if (rw[half] < 0) rw[half] = Mk * kBN;  // empty half: rows past N read as zeros
+        }
+        if (u >= C::NSV &&
+            !mbar_wait(bar(C::B_VE + sv), ((u / C::NSV) - 1) & 1, kWaitTimeoutNs)) {
           report_error(status, SPARGE_ERR_TIMEOUT);
           break;
         }
-        const int jj = min(max(__ldg(list + t), 0), Mk - 1);
-        mbar_arrive_expect_tx(bar(C::B_KF + s), C::kKV);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(s0 + C::off_k + s * C::kKV + c * kBN * 128, &tmK, bar(C::B_KF + s), c * 64,
-                      jj * kBN, bh);
-        if (t >= C::NST && !mbar_wait(bar(C::B_VE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+        mbar_arrive_expect_tx(bar(C::B_VF + sv), C::kKP);
+        for (int half = 0; half < 2; ++half)
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(s0 + C::off_v + sv * C::kKP + c * C::kChunkK + half * kBN * 128, &tmV,
+                        bar(C::B_VF + sv), c * 64, rw[half], bh);
+        if (u >= C::NSK &&
+            !mbar_wait(bar(C::B_KE + sk), ((u / C::NSK) - 1) & 1, kWaitTimeoutNs)) {
           report_error(status, SPARGE_ERR_TIMEOUT);
           break;
         }
-        mbar_arrive_expect_tx(bar(C::B_VF + s), C::kKV);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(s0 + C::off_v + s * C::kKV + c * kBN * 128, &tmV, bar(C::B_VF + s), c * 64,
-                      jj * kBN, bh);
-        issued = t + 1;
+        mbar_arrive_expect_tx(bar(C::B_KF + sk), C::kKP);
+        for (int half = 0; half < 2; ++half)
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(s0 + C::off_k + sk * C::kKP + c * C::kChunkK + half * kBN * 128, &tmK,
+                        bar(C::B_KF + sk), c * 64, rw[half], bh);
+        issued = u + 1;
       }
-      for (int t = max(0, issued - C::NST); t < issued; ++t) {
-        mbar_wait(bar(C::B_KF + t % C::NST), (t / C::NST) & 1, kWaitTimeoutNs);
-        mbar_wait(bar(C::B_VF + t % C::NST), (t / C::NST) & 1, kWaitTimeoutNs);
-      }
+      mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
+      for (int u = max(0, issued - C::NSK); u < issued; ++u)
+        mbar_wait(bar(C::B_KF + u % C::NSK), (u / C::NSK) & 1, kWaitTimeoutNs);
+      for (int u = max(0, issued - C::NSV); u < issued; ++u)
+        mbar_wait(bar(C::B_VF + u % C::NSV), (u / C::NSV) & 1, kWaitTimeoutNs);
     }
-  } else if (warp == kGIssueA) {
-    // S_t = Q K_t^T and dP_t = dO V_t^T, with Q and dO read from TMEM.
+  } else if (warp == Roles<kDqWarps>::kIssueA) {
+    // ---------------------------------------------------------- S, dP
+    // S_u = Q K_u^T into TMEM buffer u % 2 (free once dQ of step u - 2 has
+    // read its dS), then dP_u = dO V_u^T (its region frees once the compute
+    // warps have read dP of step u - 1).  M = 128 queries, N = 128 keys.
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
-      bool ok = mbar_wait(bar(C::B_QT), 0, kWaitTimeoutNs);
-      for (int t = 0; ok && t < n; ++t) {
-        const int s = t % C::NST;
-        const uint32_t dS = tmem + (t & 1) * 128;
-        // TMEM tile t & 1 holds dS(t - 2) until dQ(t - 2) has completed.
-        if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs) ||
-            (t >= 2 && !mbar_wait(bar(C::B_DSE + (t & 1)), ((t - 2) >> 1) & 1, kWaitTimeoutNs))) {
+      constexpr uint32_t idS = idesc_bf16(kBM, kPair, false, false);
+      const uint64_t dq0 = sdesc_sw128(s0 + C::off_q, 16, 1024);
+      const uint64_t ddo0 = sdesc_sw128(s0 + C::off_do, 16, 1024);
+      bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
+      for (int u = 0; ok && u < npair; ++u) {
+        const int sk = u % C::NSK, sv = u % C::NSV, b = u & 1;
+        if (!mbar_wait(bar(C::B_KF + sk), (u / C::NSK) & 1, kWaitTimeoutNs) ||
+            (u >= 2 && !mbar_wait(bar(C::B_SE + b), ((u >> 1) - 1) & 1, kWaitTimeoutNs))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t dk = sdesc_sw128(s0 + C::off_k + s * C::kKV, 16, 1024);
-        const uint64_t dv = sdesc_sw128(s0 + C::off_v + s * C::kKV, 16, 1024);
+        const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16_ta(dS, tmem + C::col_q + kk * 8, sdesc_add(dk, kko), idS, kk > 0);
+          const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
+          const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+          tc_mma_bf16(tmem + C::col_s + 128 * b, sdesc_add(dq0, ka), sdesc_add(dkd, kb), idS,
+                      kk > 0);
         }
-        if (!mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs)) {
+        tc_commit(bar(C::B_SF + b));
+        if (!mbar_wait(bar(C::B_VF + sv), (u / C::NSV) & 1, kWaitTimeoutNs) ||
+            (u >= 1 && !mbar_wait(bar(C::B_DPE), (u - 1) & 1, kWaitTimeoutNs))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint64_t dvd = sdesc_sw128(s0 + C::off_v + sv * C::kKP, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t kko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          tc_mma_bf16_ta(dS + 64, tmem + C::col_do + kk * 8, sdesc_add(dv, kko), idS, kk > 0);
+          const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
+          const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+          tc_mma_bf16(tmem + C::col_dp, sdesc_add(ddo0, ka), sdesc_add(dvd, kb), idS, kk > 0);
         }
-        tc_commit(bar(C::B_SF + (t & 1)));
-        tc_commit(bar(C::B_VE + s));
+        tc_commit(bar(C::B_DPF));
+        tc_commit(bar(C::B_VE + sv));
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
-  } else if (warp == kGIssueB) {
-    // dQ += dS_u K_u (A = dS_u from TMEM, K = 64 keys; B = K_u MN-major, N = d).
+  } else if (warp == Roles<kDqWarps>::kIssueB) {
+    // ---------------------------------------------------------- dQ
+    // dQ += dS_u K_u (A = dS from TMEM buffer u % 2, K = 128 keys; B = the key
+    // tile read MN-major, N = d).  dS of keys 16kk .. 16kk + 15 sits in the
+    // buffer's columns 32 (kk / 2) + 8 (kk % 2) .. + 7.
     if (lane == 0 && n > 0) {
       constexpr uint32_t idQ = idesc_bf16(kBM, D, false, true);
       bool ok = true;
-      for (int u = 0; ok && u < n; ++u) {
-        const int su = u % C::NST;
-        if (!mbar_wait(bar(C::B_DSF + (u & 1)), (u >> 1) & 1, kWaitTimeoutNs)) {
+      for (int u = 0; ok && u < npair; ++u) {
+        const int sk = u % C::NSK, b = u & 1;
+        if (!mbar_wait(bar(C::B_DSF + b), (u >> 1) & 1, kWaitTimeoutNs)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t ads = tmem + (u & 1) * 128 + C::col_ds;
-        const uint64_t dk = sdesc_sw128(s0 + C::off_k + su * C::kKV, kBN * 128, 1024);
+        const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, C::kChunkK, 1024);
+        const uint32_t ads = tmem + C::col_s + 128 * b;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          tc_mma_bf16_ta(tmem + C::col_dq, ads + kk * 8, sdesc_add(dk, kk * 2048), idQ,
-                         (u > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(C::B_KE + su));
-        tc_commit(bar(C::B_DSE + (u & 1)));
+        for (int kk = 0; kk < kPair / 16; ++kk)
+          tc_mma_bf16_ta(tmem + C::col_dq, ads + (kk >> 1) * 32 + (kk & 1) * 8,
+                         sdesc_add(dkd, kk * 2048), idQ, (u > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(C::B_SE + b));
+        tc_commit(bar(C::B_KE + sk));
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
   } else {
-    const int quarter = warp & 3, half = warp >> 2;
+    // ---------------------------------------------------------- compute
+    // Thread = query row r (TMEM lane); warp group g = warp / 4 takes keys
+    // 32g .. 32g + 31 of each step (64-key half g / 2 of it).
+    const int quarter = warp & 3, cg = warp >> 2, half = cg >> 1;
     const int r = quarter * 32 + lane;
-    const int c0 = half * 32;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int row = qb * kBM + r;
     const bool rv = row < N;
     const float lse2 = (rv && n > 0) ? __ldg(lse + (long long)bh * N + row) * kLog2e : 0.f;
     const float drow = rv ? __ldg(delta + (long long)bh * N + row) : 0.f;
     bool ok = true;
-    // Q and dO into TMEM (this thread's half row of each), for the S and dP
-    // MMAs of every tile.
-    if (n > 0) {
-      ok = warp_wait(bar(C::B_Q), 0);
-      if (ok) {
-        tile_half_row_to_tmem<D>(sm + C::off_q, r, half, lane_base + C::col_q);
-        tile_half_row_to_tmem<D>(sm + C::off_do, r, half, lane_base + C::col_do);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_QT));
-      }
-    }
-    int j_next = n > 0 ? min(max(__ldg(list), 0), Mk - 1) : 0;  // one tile ahead
-    for (int t = 0; ok && t < n; ++t) {
-      const int jj = j_next;
-      if (t + 1 < n) j_next = min(max(__ldg(list + t + 1), 0), Mk - 1);
-      const int kv_valid = N - jj * kBN;
-      if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
+    int rw_next = n > 0 ? half_row(0, half) : -1;  // one step ahead
+    for (int u = 0; ok && u < npair; ++u) {
+      const int b = u & 1;
+      const int rw = rw_next;
+      if (u + 1 < npair) rw_next = half_row(u + 1, half);
+      // Valid keys among this thread's 32 (0 for an empty half; warp-uniform).
+      const int valid = rw < 0 ? 0 : min(32, max(0, N - rw - 32 * (cg & 1)));
+      if (!warp_wait(bar(C::B_SF + b), (u >> 1) & 1) || !warp_wait(bar(C::B_DPF), u & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // dP first, so that its region is released (and dP of the next step
+      // computed) while this step's softmax runs.
+      uint32_t dr[16], dr2[16], sr[16], sr2[16];
+      tmem_ld32u(lane_base + C::col_dp + 32 * cg, dr, dr2);
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DPE));
+      const uint32_t sb = lane_base + C::col_s + 128 * b + 32 * cg;
+      tmem_ld32u(sb, sr, sr2);
       uint32_t pk[16];
-      {
-        float s[32], dp[32];
-        tmem_ld32(lane_base + (t & 1) * 128 + c0, s);
-        tmem_ld32(lane_base + (t & 1) * 128 + 64 + c0, dp);
+      if (rv && valid == 32) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float p0 = ex2_approx(fmaf(s[c], scale_log2, -lse2));
-          float p1 = ex2_approx(fmaf(s[c + 1], scale_log2, -lse2));
-          if (!rv || c0 + c >= kv_valid) p0 = 0.f;
-          if (!rv || c0 + c + 1 >= kv_valid) p1 = 0.f;
-          pk[c / 2] = pack_bf16x2(p0 * (dp[c] - drow), p1 * (dp[c + 1] - drow));
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e] : sr2[e - 16]),
+                                           scale_log2, -lse2));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e + 1] : sr2[e - 15]),
+                                           scale_log2, -lse2));
+          const float d_a = __uint_as_float(e < 16 ? dr[e] : dr2[e - 16]);
+          const float d_b = __uint_as_float(e < 16 ? dr[e + 1] : dr2[e - 15]);
+          pk[e / 2] = pack_bf16x2(p0 * (d_a - drow), p1 * (d_b - drow));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e] : sr2[e - 16]), scale_log2,
+                                     -lse2));
+          float p1 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e + 1] : sr2[e - 15]),
+                                     scale_log2, -lse2));
+          if (!rv || e >= valid) p0 = 0.f;
+          if (!rv || e + 1 >= valid) p1 = 0.f;
+          const float d_a = __uint_as_float(e < 16 ? dr[e] : dr2[e - 16]);
+          const float d_b = __uint_as_float(e < 16 ? dr[e + 1] : dr2[e - 15]);
+          pk[e / 2] = pack_bf16x2(p0 * (d_a - drow), p1 * (d_b - drow));
         }
       }
-      // dS_t over columns col_ds + 16 * half .. + 15 of S_t's tile (this
-      // warp's own S columns, already read into registers above).
-      {
-        const uint32_t da = lane_base + (t & 1) * 128 + C::col_ds + half * 16;
-        SPARGE_TMEM_ST_X16(da, pk);
-        tmem_st_wait();
-      }
+      // dS over the first 16 of the 32 S columns this thread read.
+      SPARGE_TMEM_ST_X16(sb, pk);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::B_DSF + (t & 1)));
+      mbar_arrive(bar(C::B_DSF + b));
     }
     if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
     bool have = ok && n > 0;
     if (have) {
-      have = warp_wait(bar(C::B_DSE + ((n - 1) & 1)), ((n - 1) >> 1) & 1);
+      const int lb = (npair - 1) & 1;
+      have = warp_wait(bar(C::B_SE + lb), ((npair - 1) >> 1) & 1);
       if (!have) report_error(status, SPARGE_ERR_TIMEOUT);
     }
     tc_fence_after();
     __nv_bfloat16* qrow = dq + ((long long)bh * N + row) * D;
 #pragma unroll 1
-    for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 16) {
+    for (int cc = cg * (D / 4); cc < (cg + 1) * (D / 4); cc += 16) {
       uint32_t ro[16];
       if (have) {
         SPARGE_TMEM_LD_X16(lane_base + C::col_dq + cc, ro);
@@ -753,14 +956,14 @@ __global__ void __launch_bounds__(kGradThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kGIssueA) {
+  if (warp == Roles<kDqWarps>::kIssueA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::tmem_cols);
     // Started early beside the dK/dV grid: the grid completes only after that
-  // one has, so work after this call sees dK and dV written.
-  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
+    // one has, so work after this call sees dK and dV written.
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == Roles<kDqWarps>::kIssueA * 32)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
 }
 
 template <int D>
@@ -773,30 +976,35 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   float* delta = ws.delta;
   const long long rows = (long long)g.BH * g.N;
   constexpr int RPB = 256 / (D / 8);
-  // D per token, and (two more CTAs) the launch orders of the gradient
-  // kernels: longest lists first, kv-blocks by CSC count, q-blocks by CSR count.
+  // Key tiles of 128 keys: pairs of 64-key kv-blocks, or 128-key blocks.
+  const int kv_per_tile = g.bk == 64 ? 2 : 1;
+  const int Mt = (g.Mk + kv_per_tile - 1) / kv_per_tile;
   const unsigned ndelta = static_cast<unsigned>((rows + RPB - 1) / RPB);
   bwd_delta_kernel<D><<<ndelta + 2, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), rows, delta,
-      ndelta, col_cnt, g.BH * g.Mk, ws.col_order, row_cnt, g.BH * g.Mq, ws.row_order);
+      col_cnt, g.BH, g.Mk, Mt, kv_per_tile, ws.col_order, row_cnt, g.BH * g.Mq, ws.row_order);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  CUtensorMap tq, tk, tv, tdo;
+  // Q and dO in 128-row boxes for the dQ kernel, 64-row boxes (query
+  // halves) for the dK/dV kernel; K and V in 64-row boxes.
+  CUtensorMap tq, tk, tv, tdo, tq64, tdo64;
   if (make_tmap_bf16(&tq, q, g.BH, g.N, D, kBM) != 0 || make_tmap_bf16(&tk, k, g.BH, g.N, D, kBN) != 0 ||
       make_tmap_bf16(&tv, v, g.BH, g.N, D, kBN) != 0 ||
-      make_tmap_bf16(&tdo, dout, g.BH, g.N, D, kBM) != 0)
+      make_tmap_bf16(&tdo, dout, g.BH, g.N, D, kBM) != 0 ||
+      make_tmap_bf16(&tq64, q, g.BH, g.N, D, 64) != 0 ||
+      make_tmap_bf16(&tdo64, dout, g.BH, g.N, D, 64) != 0)
     return cudaErrorInvalidValue;
   const float scale_log2 = scale * kLog2e;
 
   e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DkdvCfg<D>::smem_alloc);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<D><<<static_cast<unsigned>((long long)g.BH * g.Mk), kGradThreads,
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>((long long)g.BH * Mt), Roles<kDkdvWarps>::kThreads,
                        DkdvCfg<D>::smem_alloc, st>>>(
-      tq, tk, tv, tdo, lse, delta, col_idx, col_cnt, ws.col_order, g.N, g.Mq, g.Mk, scale,
-      scale_log2,
-      static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), status);
+      tq64, tk, tv, tdo64, lse, delta, col_idx, col_cnt, ws.col_order, g.N, g.Mq, g.Mk, Mt,
+      kv_per_tile, scale, scale_log2, static_cast<__nv_bfloat16*>(dk),
+      static_cast<__nv_bfloat16*>(dv), status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -807,7 +1015,7 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   // CTAs run (D and the launch orders were complete before dK/dV started).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((long long)g.BH * g.Mq));
-  cfg.blockDim = dim3(kGradThreads);
+  cfg.blockDim = dim3(Roles<kDqWarps>::kThreads);
   cfg.dynamicSmemBytes = DqCfg<D>::smem_alloc;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -817,8 +1025,9 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D>, tq, tk, tv, tdo, lse,
                             static_cast<const float*>(delta), row_idx, row_cnt,
-                            static_cast<const int32_t*>(ws.row_order), g.N, g.Mq, g.Mk, scale,
-                            scale_log2, static_cast<__nv_bfloat16*>(dq), status);
+                            static_cast<const int32_t*>(ws.row_order), g.N, g.Mq, g.Mk,
+                            g.bk == 64 ? 1 : 2, scale, scale_log2,
+                            static_cast<__nv_bfloat16*>(dq), status);
 }
 
 }  // namespace

@@ -55,6 +55,11 @@ SPARGE_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
       "r"(bytes)
       : "memory");
 }
+// Adds `bytes` to the transaction count of the current phase (no arrival).
+SPARGE_DEV void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
 SPARGE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -232,6 +237,12 @@ SPARGE_DEV void tmem_ld32(uint32_t addr, float (&x)[32]) {
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),     \
       "r"(r[15])                                                                            \
       : "memory")
+
+#define SPARGE_TMEM_ST_X8(taddr, r)                                                         \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), \
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),       \
+               "r"(r[7])                                                                          \
+               : "memory")
 
 SPARGE_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
