@@ -115,8 +115,10 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, long long rows,
     float* __restrict__ delta, const int32_t* __restrict__ col_cnt, int BH, int Mk, int Mt,
     int kv_per_tile, int32_t* __restrict__ tile_order, const int32_t* __restrict__ row_cnt,
-    int nrow, int32_t* __restrict__ row_order) {
+    int nrow, int32_t* __restrict__ row_order, int32_t* __restrict__ work) {
   if (blockIdx.x < 2) {
+    // The work counters of the persistent gradient kernels start at zero.
+    if (blockIdx.x == 0 && threadIdx.x < 4) work[threadIdx.x] = 0;
     if (blockIdx.x == 0) {
       auto work = [&](int it) -> long long {
         const int bh = it / Mt, jt = it % Mt;
@@ -645,6 +647,7 @@ struct DqCfg {
   // slot only until dP.
   static constexpr int NSK = D == 128 ? 3 : 6;
   static constexpr int NSV = D == 128 ? 2 : 4;
+  static constexpr int NRING = 4;                   // q-blocks handed out ahead
   static constexpr uint32_t kKP = kPair * D * 2;    // K (or V) of 128 keys
   static constexpr uint32_t kQ = kBM * D * 2;
   static constexpr uint32_t kChunkK = kPair * 128;
@@ -653,24 +656,29 @@ struct DqCfg {
   static constexpr uint32_t off_do = off_q + kQ;
   static constexpr uint32_t off_k = off_do + kQ;        // NSK slots of K
   static constexpr uint32_t off_v = off_k + NSK * kKP;  // NSV slots of V
-  static constexpr uint32_t off_bar = off_v + NSV * kKP;
-  static constexpr int B_Q = 0;            // Q, dO landed
-  static constexpr int B_KF = 1;           // NSK: K landed
+  static constexpr uint32_t off_ring = off_v + NSV * kKP;  // NRING q-block ids
+  static constexpr uint32_t off_bar = off_ring + 64;
+  static constexpr int B_Q = 0;            // Q, dO of a q-block landed
+  static constexpr int B_QE = 1;           // its S and dP MMAs done: Q, dO slots free
+  static constexpr int B_KF = 2;           // NSK: K landed
   static constexpr int B_VF = B_KF + NSK;  // NSV: V landed
   static constexpr int B_KE = B_VF + NSV;  // NSK: K slot free (dQ of its step done)
   static constexpr int B_VE = B_KE + NSK;  // NSV: V slot free (dP of its step done)
   static constexpr int B_SF = B_VE + NSV;  // 2: S in TMEM buffer b
   static constexpr int B_SE = B_SF + 2;    // 2: dQ read dS of buffer b (buffer free)
-  static constexpr int B_DSF = B_SE + 2;   // 2, count 256: dS written into buffer b
+  static constexpr int B_DSF = B_SE + 2;   // 2, all compute threads: dS written into buffer b
   static constexpr int B_DPF = B_DSF + 2;  // dP complete
-  static constexpr int B_DPE = B_DPF + 1;  // dP read by every compute thread (count 256)
-  static constexpr int B_DONE = B_DPE + 1; // count 2
+  static constexpr int B_DPE = B_DPF + 1;  // all compute threads: dP read
+  static constexpr int B_DQE = B_DPE + 1;  // all compute threads: dQ accumulator read out
+  static constexpr int B_IF = B_DQE + 1;   // NRING: q-block id written
+  static constexpr int B_IE = B_IF + NRING;  // NRING: id read by both issuers and every compute warp
+  static constexpr int B_DONE = B_IE + NRING;  // count 2
   static constexpr int NBAR = B_DONE + 1;
   static constexpr uint32_t off_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_slot + 16;
   static constexpr uint32_t smem_alloc = bytes + 1024;
-  // TMEM: dQ [0, D), S of step u in buffer u % 2 at 128 + 128 * (u % 2) (128
-  // keys; dS of keys 32g .. 32g + 31 written over its columns 32g .. 32g + 15
+  // TMEM: dQ [0, D), S of step g in buffer g % 2 at 128 + 128 * (g % 2) (128
+  // keys; dS of keys 32c .. 32c + 31 written over its columns 32c .. 32c + 15
   // as bf16 pairs), dP at 384.
   static constexpr uint32_t tmem_cols = 512;
   static constexpr uint32_t col_dq = 0;
@@ -678,56 +686,50 @@ struct DqCfg {
   static constexpr uint32_t col_dp = 384;
 };
 
-// One CTA per q-block.  Its list of kept kv-blocks is taken two entries at a
-// time (kv_per_entry = 1: 64-key blocks; the second of an odd count is
-// empty), or one 128-key block per step (kv_per_entry = 2).  Q and dO stay in
-// shared memory as the A operands of S and dP; S is double-buffered in TMEM,
-// so S of the next step is computed while the compute warps work on this one.
+// Persistent: one CTA per SM takes q-blocks from a work counter, in the
+// launch order (long lists first), until all are done.  A q-block's list of
+// kept kv-blocks is taken two entries at a time (kv_per_entry = 1: 64-key
+// blocks; the second of an odd count is empty), or one 128-key block per step
+// (kv_per_entry = 2).  Q and dO stay in shared memory as the A operands of S
+// and dP; S is double-buffered in TMEM, so S of the next step is computed
+// while the compute warps work on this one, and the loads and first MMAs of
+// the next q-block overlap the current one's last steps and epilogue.  The
+// steps of successive q-blocks share one running step count g, which indexes
+// the slot rings and barrier phases.
 template <int D>
 __global__ void __launch_bounds__(Roles<kDqWarps>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const float* __restrict__ lse, const float* __restrict__ delta,
                   const int32_t* __restrict__ row_idx, const int32_t* __restrict__ row_cnt,
-                  const int32_t* __restrict__ row_order, int N, int Mq, int Mk, int kv_per_entry,
-                  float scale, float scale_log2, __nv_bfloat16* __restrict__ dq,
-                  int32_t* __restrict__ status) {
+                  const int32_t* __restrict__ row_order, int nitems, int32_t* __restrict__ work,
+                  int N, int Mq, int Mk, int kv_per_entry, float scale, float scale_log2,
+                  __nv_bfloat16* __restrict__ dq, int32_t* __restrict__ status) {
   using C = DqCfg<D>;
+  using R = Roles<kDqWarps>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const uint32_t s0 = smem_u32(sm);
   auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
+  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(sm + C::off_ring);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = min(max(__ldg(row_order + blockIdx.x), 0), static_cast<int>(gridDim.x) - 1);
-  const int bh = item / Mq;
-  const int qb = item % Mq;
-  const long long row_id = (long long)bh * Mq + qb;
-  const int n = min(max(__ldg(row_cnt + row_id), 0), Mk);
-  const int32_t* list = row_idx + row_id * Mk;
   const bool single = kv_per_entry == 1;
-  const int npair = single ? (n + 1) / 2 : n;
-  // First row (in tokens) of the two 64-key halves of step u; -1 = empty half.
-  auto half_row = [&](int u, int half) -> int {
-    if (single) {
-      const int e = 2 * u + half;
-      return e < n ? min(max(__ldg(list + e), 0), Mk - 1) * kBN : -1;
-    }
-    return min(max(__ldg(list + u), 0), Mk - 1) * kPair + half * kBN;
-  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == C::B_DPE || i == C::B_DSF || i == C::B_DSF + 1) cnt = 32 * Roles<kDqWarps>::kCompute;
+      if (i == C::B_DPE || i == C::B_DQE || i == C::B_DSF || i == C::B_DSF + 1)
+        cnt = 32 * R::kCompute;
+      if (i >= C::B_IE && i < C::B_IE + C::NRING) cnt = 2 + R::kCompute;
       if (i == C::B_DONE) cnt = 2;
       mbar_init(bar(i), cnt);
     }
     fence_barrier_init();
   }
-  if (warp == Roles<kDqWarps>::kIssueA) {
+  if (warp == R::kIssueA) {
     tmem_alloc(smem_u32(slot), C::tmem_cols);
     tmem_relinquish();
   }
@@ -736,232 +738,338 @@ __global__ void __launch_bounds__(Roles<kDqWarps>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *slot;
 
-  if (warp == Roles<kDqWarps>::kProducer) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::kQ);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(s0 + C::off_q + c * C::kChunkQ, &tmQ, bar(C::B_Q), c * 64, qb * kBM, bh);
-        tma_load_3d(s0 + C::off_do + c * C::kChunkQ, &tmDO, bar(C::B_Q), c * 64, qb * kBM, bh);
-      }
-      int issued = 0;
-      for (int u = 0; u < npair; ++u) {
-        const int sk = u % C::NSK, sv = u % C::NSV;
-        int rw[2];
-        for (int half = 0; half < 2; ++half) {
-          rw[half] = half_row(u, half);
-          if (rw[half] < 0) rw[half] = Mk * kBN;  // empty half: rows past N read as zeros
-        }
-        if (u >= C::NSV &&
-            !mbar_wait(bar(C::B_VE + sv), ((u / C::NSV) - 1) & 1, kWaitTimeoutNs)) {
-          report_error(status, SPARGE_ERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(bar(C::B_VF + sv), C::kKP);
-        for (int half = 0; half < 2; ++half)
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(s0 + C::off_v + sv * C::kKP + c * C::kChunkK + half * kBN * 128, &tmV,
-                        bar(C::B_VF + sv), c * 64, rw[half], bh);
-        if (u >= C::NSK &&
-            !mbar_wait(bar(C::B_KE + sk), ((u / C::NSK) - 1) & 1, kWaitTimeoutNs)) {
-          report_error(status, SPARGE_ERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(bar(C::B_KF + sk), C::kKP);
-        for (int half = 0; half < 2; ++half)
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(s0 + C::off_k + sk * C::kKP + c * C::kChunkK + half * kBN * 128, &tmK,
-                        bar(C::B_KF + sk), c * 64, rw[half], bh);
-        issued = u + 1;
-      }
-      mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
-      for (int u = max(0, issued - C::NSK); u < issued; ++u)
-        mbar_wait(bar(C::B_KF + u % C::NSK), (u / C::NSK) & 1, kWaitTimeoutNs);
-      for (int u = max(0, issued - C::NSV); u < issued; ++u)
-        mbar_wait(bar(C::B_VF + u % C::NSV), (u / C::NSV) & 1, kWaitTimeoutNs);
+  // The q-block handed out as the seq-th of this CTA (-1: no more work).  The
+  // producer fetches ids from the counter into a ring; the other roles read
+  // them from there, in the same order.
+  auto next_item = [&](int seq, bool ok) -> int {
+    const int rs = seq % C::NRING;
+    if (!ok || !mbar_wait(bar(C::B_IF + rs), (seq / C::NRING) & 1, kWaitTimeoutNs)) return -2;
+    const int it = ring[rs];
+    return it;
+  };
+  auto release_item = [&](int seq) { mbar_arrive(bar(C::B_IE + seq % C::NRING)); };
+  struct Item {
+    int bh, qb, n, npair;
+    const int32_t* list;
+  };
+  auto item_info = [&](int it) -> Item {
+    Item x;
+    x.bh = it / Mq;
+    x.qb = it % Mq;
+    const long long row_id = (long long)x.bh * Mq + x.qb;
+    x.n = min(max(__ldg(row_cnt + row_id), 0), Mk);
+    x.list = row_idx + row_id * Mk;
+    x.npair = single ? (x.n + 1) / 2 : x.n;
+    return x;
+  };
+  // First row (in tokens) of the two 64-key halves of step u; -1 = empty half.
+  auto half_row = [&](const Item& x, int u, int half) -> int {
+    if (single) {
+      const int e = 2 * u + half;
+      return e < x.n ? min(max(__ldg(x.list + e), 0), Mk - 1) * kBN : -1;
     }
-  } else if (warp == Roles<kDqWarps>::kIssueA) {
+    return min(max(__ldg(x.list + u), 0), Mk - 1) * kPair + half * kBN;
+  };
+
+  if (warp == R::kProducer) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int g = 0, j = 0;
+      bool ok = true;
+      for (int seq = 0;; ++seq) {
+        const int rs = seq % C::NRING;
+        if (seq >= C::NRING &&
+            !mbar_wait(bar(C::B_IE + rs), ((seq / C::NRING) - 1) & 1, kWaitTimeoutNs))
+          ok = false;
+        int it = -1;
+        if (ok) {
+          const int k = atomicAdd(work, 1);
+          it = k < nitems ? min(max(__ldg(row_order + k), 0), nitems - 1) : -1;
+        }
+        ring[rs] = ok ? it : -2;
+        mbar_arrive(bar(C::B_IF + rs));
+        if (it < 0) break;
+        const Item x = item_info(it);
+        if (x.n == 0) continue;
+        if (j >= 1 && !mbar_wait(bar(C::B_QE), (j - 1) & 1, kWaitTimeoutNs)) {
+          ok = false;
+          continue;  // publishes the failure in the next ring slot, then stops
+        }
+        mbar_arrive_expect_tx(bar(C::B_Q), 2 * C::kQ);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(s0 + C::off_q + c * C::kChunkQ, &tmQ, bar(C::B_Q), c * 64, x.qb * kBM, x.bh);
+          tma_load_3d(s0 + C::off_do + c * C::kChunkQ, &tmDO, bar(C::B_Q), c * 64, x.qb * kBM,
+                      x.bh);
+        }
+        ++j;
+        for (int u = 0; ok && u < x.npair; ++u, ++g) {
+          const int sk = g % C::NSK, sv = g % C::NSV;
+          int rw[2];
+          for (int half = 0; half < 2; ++half) {
+            rw[half] = half_row(x, u, half);
+            if (rw[half] < 0) rw[half] = Mk * kBN;  // empty half: rows past N read as zeros
+          }
+          if (g >= C::NSV &&
+              !mbar_wait(bar(C::B_VE + sv), ((g / C::NSV) - 1) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::B_VF + sv), C::kKP);
+          for (int half = 0; half < 2; ++half)
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(s0 + C::off_v + sv * C::kKP + c * C::kChunkK + half * kBN * 128, &tmV,
+                          bar(C::B_VF + sv), c * 64, rw[half], x.bh);
+          if (g >= C::NSK &&
+              !mbar_wait(bar(C::B_KE + sk), ((g / C::NSK) - 1) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::B_KF + sk), C::kKP);
+          for (int half = 0; half < 2; ++half)
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(s0 + C::off_k + sk * C::kKP + c * C::kChunkK + half * kBN * 128, &tmK,
+                          bar(C::B_KF + sk), c * 64, rw[half], x.bh);
+        }
+      }
+      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
+      // Let the last loads land before the CTA can exit.
+      if (j > 0) mbar_wait(bar(C::B_Q), (j - 1) & 1, kWaitTimeoutNs);
+      for (int e = max(0, g - C::NSK); e < g; ++e)
+        mbar_wait(bar(C::B_KF + e % C::NSK), (e / C::NSK) & 1, kWaitTimeoutNs);
+      for (int e = max(0, g - C::NSV); e < g; ++e)
+        mbar_wait(bar(C::B_VF + e % C::NSV), (e / C::NSV) & 1, kWaitTimeoutNs);
+    }
+  } else if (warp == R::kIssueA) {
     // ---------------------------------------------------------- S, dP
-    // S_u = Q K_u^T into TMEM buffer u % 2 (free once dQ of step u - 2 has
-    // read its dS), then dP_u = dO V_u^T (its region frees once the compute
-    // warps have read dP of step u - 1).  M = 128 queries, N = 128 keys.
-    if (lane == 0 && n > 0) {
+    // S_g = Q K_g^T into TMEM buffer g % 2 (free once dQ of step g - 2 has
+    // read its dS), then dP_g = dO V_g^T (its region frees once the compute
+    // warps have read dP of step g - 1).  M = 128 queries, N = 128 keys.
+    if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kPair, false, false);
       const uint64_t dq0 = sdesc_sw128(s0 + C::off_q, 16, 1024);
       const uint64_t ddo0 = sdesc_sw128(s0 + C::off_do, 16, 1024);
-      bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
-      for (int u = 0; ok && u < npair; ++u) {
-        const int sk = u % C::NSK, sv = u % C::NSV, b = u & 1;
-        if (!mbar_wait(bar(C::B_KF + sk), (u / C::NSK) & 1, kWaitTimeoutNs) ||
-            (u >= 2 && !mbar_wait(bar(C::B_SE + b), ((u >> 1) - 1) & 1, kWaitTimeoutNs))) {
+      bool ok = true;
+      int g = 0, j = 0;
+      for (int seq = 0;; ++seq) {
+        const int it = next_item(seq, ok);
+        release_item(seq);
+        if (it < 0) {
+          if (it == -2) ok = false;
+          break;
+        }
+        const Item x = item_info(it);
+        if (x.n == 0) continue;
+        if (!mbar_wait(bar(C::B_Q), j & 1, kWaitTimeoutNs)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, 16, 1024);
+        ++j;
+        for (int u = 0; ok && u < x.npair; ++u, ++g) {
+          const int sk = g % C::NSK, sv = g % C::NSV, b = g & 1;
+          if (!mbar_wait(bar(C::B_KF + sk), (g / C::NSK) & 1, kWaitTimeoutNs) ||
+              (g >= 2 && !mbar_wait(bar(C::B_SE + b), ((g >> 1) - 1) & 1, kWaitTimeoutNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
-          const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
-          tc_mma_bf16(tmem + C::col_s + 128 * b, sdesc_add(dq0, ka), sdesc_add(dkd, kb), idS,
-                      kk > 0);
-        }
-        tc_commit(bar(C::B_SF + b));
-        if (!mbar_wait(bar(C::B_VF + sv), (u / C::NSV) & 1, kWaitTimeoutNs) ||
-            (u >= 1 && !mbar_wait(bar(C::B_DPE), (u - 1) & 1, kWaitTimeoutNs))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t dvd = sdesc_sw128(s0 + C::off_v + sv * C::kKP, 16, 1024);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
+            const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+            tc_mma_bf16(tmem + C::col_s + 128 * b, sdesc_add(dq0, ka), sdesc_add(dkd, kb), idS,
+                        kk > 0);
+          }
+          tc_commit(bar(C::B_SF + b));
+          if (!mbar_wait(bar(C::B_VF + sv), (g / C::NSV) & 1, kWaitTimeoutNs) ||
+              (g >= 1 && !mbar_wait(bar(C::B_DPE), (g - 1) & 1, kWaitTimeoutNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dvd = sdesc_sw128(s0 + C::off_v + sv * C::kKP, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
-          const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
-          tc_mma_bf16(tmem + C::col_dp, sdesc_add(ddo0, ka), sdesc_add(dvd, kb), idS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
+            const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+            tc_mma_bf16(tmem + C::col_dp, sdesc_add(ddo0, ka), sdesc_add(dvd, kb), idS, kk > 0);
+          }
+          tc_commit(bar(C::B_DPF));
+          tc_commit(bar(C::B_VE + sv));
         }
-        tc_commit(bar(C::B_DPF));
-        tc_commit(bar(C::B_VE + sv));
+        if (!ok) break;
+        tc_commit(bar(C::B_QE));  // every S and dP of this q-block issued
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
-  } else if (warp == Roles<kDqWarps>::kIssueB) {
+  } else if (warp == R::kIssueB) {
     // ---------------------------------------------------------- dQ
-    // dQ += dS_u K_u (A = dS from TMEM buffer u % 2, K = 128 keys; B = the key
+    // dQ += dS_g K_g (A = dS from TMEM buffer g % 2, K = 128 keys; B = the key
     // tile read MN-major, N = d).  dS of keys 16kk .. 16kk + 15 sits in the
-    // buffer's columns 32 (kk / 2) + 8 (kk % 2) .. + 7.
-    if (lane == 0 && n > 0) {
+    // buffer's columns 32 (kk / 2) + 8 (kk % 2) .. + 7.  The first step of a
+    // q-block waits until the previous one's accumulator has been read out.
+    if (lane == 0) {
       constexpr uint32_t idQ = idesc_bf16(kBM, D, false, true);
       bool ok = true;
-      for (int u = 0; ok && u < npair; ++u) {
-        const int sk = u % C::NSK, b = u & 1;
-        if (!mbar_wait(bar(C::B_DSF + b), (u >> 1) & 1, kWaitTimeoutNs)) {
-          ok = false;
+      int g = 0, j = 0;
+      for (int seq = 0;; ++seq) {
+        const int it = next_item(seq, ok);
+        release_item(seq);
+        if (it < 0) {
+          if (it == -2) ok = false;
           break;
         }
-        tc_fence_after();
-        const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, C::kChunkK, 1024);
-        const uint32_t ads = tmem + C::col_s + 128 * b;
+        const Item x = item_info(it);
+        if (x.n == 0) continue;
+        for (int u = 0; ok && u < x.npair; ++u, ++g) {
+          const int sk = g % C::NSK, b = g & 1;
+          if (!mbar_wait(bar(C::B_DSF + b), (g >> 1) & 1, kWaitTimeoutNs) ||
+              (u == 0 && j >= 1 && !mbar_wait(bar(C::B_DQE), (j - 1) & 1, kWaitTimeoutNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, C::kChunkK, 1024);
+          const uint32_t ads = tmem + C::col_s + 128 * b;
 #pragma unroll
-        for (int kk = 0; kk < kPair / 16; ++kk)
-          tc_mma_bf16_ta(tmem + C::col_dq, ads + (kk >> 1) * 32 + (kk & 1) * 8,
-                         sdesc_add(dkd, kk * 2048), idQ, (u > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(C::B_SE + b));
-        tc_commit(bar(C::B_KE + sk));
+          for (int kk = 0; kk < kPair / 16; ++kk)
+            tc_mma_bf16_ta(tmem + C::col_dq, ads + (kk >> 1) * 32 + (kk & 1) * 8,
+                           sdesc_add(dkd, kk * 2048), idQ, (u > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(C::B_SE + b));
+          tc_commit(bar(C::B_KE + sk));
+        }
+        ++j;
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
-  } else {
+  } else if (warp < R::kCompute) {
     // ---------------------------------------------------------- compute
-    // Thread = query row r (TMEM lane); warp group g = warp / 4 takes keys
-    // 32g .. 32g + 31 of each step (64-key half g / 2 of it).
+    // Thread = query row r (TMEM lane); warp group c = warp / 4 takes keys
+    // 32c .. 32c + 31 of each step (64-key half c / 2 of it), and features
+    // c * D/4 .. (c + 1) * D/4 - 1 of dQ.
     const int quarter = warp & 3, cg = warp >> 2, half = cg >> 1;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int row = qb * kBM + r;
-    const bool rv = row < N;
-    const float lse2 = (rv && n > 0) ? __ldg(lse + (long long)bh * N + row) * kLog2e : 0.f;
-    const float drow = rv ? __ldg(delta + (long long)bh * N + row) : 0.f;
     bool ok = true;
-    int rw_next = n > 0 ? half_row(0, half) : -1;  // one step ahead
-    for (int u = 0; ok && u < npair; ++u) {
-      const int b = u & 1;
-      const int rw = rw_next;
-      if (u + 1 < npair) rw_next = half_row(u + 1, half);
-      // Valid keys among this thread's 32 (0 for an empty half; warp-uniform).
-      const int valid = rw < 0 ? 0 : min(32, max(0, N - rw - 32 * (cg & 1)));
-      if (!warp_wait(bar(C::B_SF + b), (u >> 1) & 1) || !warp_wait(bar(C::B_DPF), u & 1)) {
+    int g = 0, j = 0;
+    for (int seq = 0;; ++seq) {
+      const int it = next_item(seq, ok);
+      __syncwarp();
+      if (lane == 0) release_item(seq);
+      if (it < 0) {
+        if (it == -2) ok = false;
+        break;
+      }
+      const Item x = item_info(it);
+      const int row = x.qb * kBM + r;
+      const bool rv = row < N;
+      __nv_bfloat16* qrow = dq + ((long long)x.bh * N + row) * D;
+      if (x.n == 0) {
+        if (rv) {
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          for (int cc = cg * (D / 4); cc < (cg + 1) * (D / 4); cc += 8)
+            __stcs(reinterpret_cast<uint4*>(qrow + cc), z);
+        }
+        continue;
+      }
+      const float lse2 = rv ? __ldg(lse + (long long)x.bh * N + row) * kLog2e : 0.f;
+      const float drow = rv ? __ldg(delta + (long long)x.bh * N + row) : 0.f;
+      int rw_next = half_row(x, 0, half);  // one step ahead
+      for (int u = 0; ok && u < x.npair; ++u, ++g) {
+        const int b = g & 1;
+        const int rw = rw_next;
+        if (u + 1 < x.npair) rw_next = half_row(x, u + 1, half);
+        // Valid keys among this thread's 32 (0 for an empty half; warp-uniform).
+        const int valid = rw < 0 ? 0 : min(32, max(0, N - rw - 32 * (cg & 1)));
+        if (!warp_wait(bar(C::B_SF + b), (g >> 1) & 1) || !warp_wait(bar(C::B_DPF), g & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dP first, so that its region is released (and dP of the next step
+        // computed) while this step's softmax runs.
+        uint32_t dr[16], dr2[16], sr[16], sr2[16];
+        tmem_ld32u(lane_base + C::col_dp + 32 * cg, dr, dr2);
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DPE));
+        const uint32_t sb = lane_base + C::col_s + 128 * b + 32 * cg;
+        tmem_ld32u(sb, sr, sr2);
+        uint32_t pk[16];
+        if (rv && valid == 32) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e] : sr2[e - 16]),
+                                             scale_log2, -lse2));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e + 1] : sr2[e - 15]),
+                                             scale_log2, -lse2));
+            const float d_a = __uint_as_float(e < 16 ? dr[e] : dr2[e - 16]);
+            const float d_b = __uint_as_float(e < 16 ? dr[e + 1] : dr2[e - 15]);
+            pk[e / 2] = pack_bf16x2(p0 * (d_a - drow), p1 * (d_b - drow));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float p0 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e] : sr2[e - 16]), scale_log2,
+                                       -lse2));
+            float p1 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e + 1] : sr2[e - 15]),
+                                       scale_log2, -lse2));
+            if (!rv || e >= valid) p0 = 0.f;
+            if (!rv || e + 1 >= valid) p1 = 0.f;
+            const float d_a = __uint_as_float(e < 16 ? dr[e] : dr2[e - 16]);
+            const float d_b = __uint_as_float(e < 16 ? dr[e + 1] : dr2[e - 15]);
+            pk[e / 2] = pack_bf16x2(p0 * (d_a - drow), p1 * (d_b - drow));
+          }
+        }
+        // dS over the first 16 of the 32 S columns this thread read.
+        SPARGE_TMEM_ST_X16(sb, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DSF + b));
+      }
+      if (!ok) break;
+      // Epilogue: read this warp's dQ columns, release the accumulator to the
+      // next q-block's dQ MMAs, then scale, convert and store.
+      const int gl = g - 1;
+      if (!warp_wait(bar(C::B_SE + (gl & 1)), (gl >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // dP first, so that its region is released (and dP of the next step
-      // computed) while this step's softmax runs.
-      uint32_t dr[16], dr2[16], sr[16], sr2[16];
-      tmem_ld32u(lane_base + C::col_dp + 32 * cg, dr, dr2);
+      uint32_t ro[D / 4];
+#pragma unroll
+      for (int c = 0; c < D / 4; c += 16) SPARGE_TMEM_LD_X16(lane_base + C::col_dq + cg * (D / 4) + c, (ro + c));
+#pragma unroll
+      for (int c = 0; c < D / 4; c += 16) SPARGE_TMEM_WAIT_LD16((ro + c));
       tc_fence_before();
-      mbar_arrive(bar(C::B_DPE));
-      const uint32_t sb = lane_base + C::col_s + 128 * b + 32 * cg;
-      tmem_ld32u(sb, sr, sr2);
-      uint32_t pk[16];
-      if (rv && valid == 32) {
+      mbar_arrive(bar(C::B_DQE));
+      ++j;
+      if (rv) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e] : sr2[e - 16]),
-                                           scale_log2, -lse2));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e + 1] : sr2[e - 15]),
-                                           scale_log2, -lse2));
-          const float d_a = __uint_as_float(e < 16 ? dr[e] : dr2[e - 16]);
-          const float d_b = __uint_as_float(e < 16 ? dr[e + 1] : dr2[e - 15]);
-          pk[e / 2] = pack_bf16x2(p0 * (d_a - drow), p1 * (d_b - drow));
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e] : sr2[e - 16]), scale_log2,
-                                     -lse2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e + 1] : sr2[e - 15]),
-                                     scale_log2, -lse2));
-          if (!rv || e >= valid) p0 = 0.f;
-          if (!rv || e + 1 >= valid) p1 = 0.f;
-          const float d_a = __uint_as_float(e < 16 ? dr[e] : dr2[e - 16]);
-          const float d_b = __uint_as_float(e < 16 ? dr[e + 1] : dr2[e - 15]);
-          pk[e / 2] = pack_bf16x2(p0 * (d_a - drow), p1 * (d_b - drow));
+        for (int c = 0; c < D / 4; c += 8) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(ro[c + 0]) * scale, __uint_as_float(ro[c + 1]) * scale);
+          w.y = pack_bf16x2(__uint_as_float(ro[c + 2]) * scale, __uint_as_float(ro[c + 3]) * scale);
+          w.z = pack_bf16x2(__uint_as_float(ro[c + 4]) * scale, __uint_as_float(ro[c + 5]) * scale);
+          w.w = pack_bf16x2(__uint_as_float(ro[c + 6]) * scale, __uint_as_float(ro[c + 7]) * scale);
+          __stcs(reinterpret_cast<uint4*>(qrow + cg * (D / 4) + c), w);
         }
       }
-      // dS over the first 16 of the 32 S columns this thread read.
-      SPARGE_TMEM_ST_X16(sb, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DSF + b));
     }
     if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-    bool have = ok && n > 0;
-    if (have) {
-      const int lb = (npair - 1) & 1;
-      have = warp_wait(bar(C::B_SE + lb), ((npair - 1) >> 1) & 1);
-      if (!have) report_error(status, SPARGE_ERR_TIMEOUT);
-    }
-    tc_fence_after();
-    __nv_bfloat16* qrow = dq + ((long long)bh * N + row) * D;
-#pragma unroll 1
-    for (int cc = cg * (D / 4); cc < (cg + 1) * (D / 4); cc += 16) {
-      uint32_t ro[16];
-      if (have) {
-        SPARGE_TMEM_LD_X16(lane_base + C::col_dq + cc, ro);
-        SPARGE_TMEM_WAIT_LD16(ro);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) ro[c] = 0u;
-      }
-      uint4 w0, w1;
-      w0.x = pack_bf16x2(__uint_as_float(ro[0]) * scale, __uint_as_float(ro[1]) * scale);
-      w0.y = pack_bf16x2(__uint_as_float(ro[2]) * scale, __uint_as_float(ro[3]) * scale);
-      w0.z = pack_bf16x2(__uint_as_float(ro[4]) * scale, __uint_as_float(ro[5]) * scale);
-      w0.w = pack_bf16x2(__uint_as_float(ro[6]) * scale, __uint_as_float(ro[7]) * scale);
-      w1.x = pack_bf16x2(__uint_as_float(ro[8]) * scale, __uint_as_float(ro[9]) * scale);
-      w1.y = pack_bf16x2(__uint_as_float(ro[10]) * scale, __uint_as_float(ro[11]) * scale);
-      w1.z = pack_bf16x2(__uint_as_float(ro[12]) * scale, __uint_as_float(ro[13]) * scale);
-      w1.w = pack_bf16x2(__uint_as_float(ro[14]) * scale, __uint_as_float(ro[15]) * scale);
-      if (rv) {
-        __stcs(reinterpret_cast<uint4*>(qrow + cc), w0);
-        __stcs(reinterpret_cast<uint4*>(qrow + cc + 8), w1);
-      }
-    }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == Roles<kDqWarps>::kIssueA) {
+  if (warp == R::kIssueA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::tmem_cols);
     // Started early beside the dK/dV grid: the grid completes only after that
     // one has, so work after this call sees dK and dV written.
-    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == Roles<kDqWarps>::kIssueA * 32)
+    if (blockIdx.x == 0 && threadIdx.x == R::kIssueA * 32)
       asm volatile("griddepcontrol.wait;" ::: "memory");
   }
 }
@@ -982,7 +1090,8 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   const unsigned ndelta = static_cast<unsigned>((rows + RPB - 1) / RPB);
   bwd_delta_kernel<D><<<ndelta + 2, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), rows, delta,
-      col_cnt, g.BH, g.Mk, Mt, kv_per_tile, ws.col_order, row_cnt, g.BH * g.Mq, ws.row_order);
+      col_cnt, g.BH, g.Mk, Mt, kv_per_tile, ws.col_order, row_cnt, g.BH * g.Mq, ws.row_order,
+      ws.work);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -1013,8 +1122,15 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: the dQ CTAs may start while the last dK/dV
   // CTAs run (D and the launch orders were complete before dK/dV started).
+  // Persistent: one CTA per SM (or per q-block when there are fewer).
+  int dev = 0, nsm = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int nq = g.BH * g.Mq;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((long long)g.BH * g.Mq));
+  cfg.gridDim = dim3(static_cast<unsigned>(max(1, min(nq, nsm))));
   cfg.blockDim = dim3(Roles<kDqWarps>::kThreads);
   cfg.dynamicSmemBytes = DqCfg<D>::smem_alloc;
   cfg.stream = st;
@@ -1025,8 +1141,8 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D>, tq, tk, tv, tdo, lse,
                             static_cast<const float*>(delta), row_idx, row_cnt,
-                            static_cast<const int32_t*>(ws.row_order), g.N, g.Mq, g.Mk,
-                            g.bk == 64 ? 1 : 2, scale, scale_log2,
+                            static_cast<const int32_t*>(ws.row_order), nq, ws.work, g.N, g.Mq,
+                            g.Mk, g.bk == 64 ? 1 : 2, scale, scale_log2,
                             static_cast<__nv_bfloat16*>(dq), status);
 }
 
@@ -1051,7 +1167,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 size_t bwd_workspace_bytes(const Geom& g) {
   return align256((size_t)g.BH * g.N * sizeof(float)) +
          align256((size_t)g.BH * g.Mk * sizeof(int32_t)) +
-         align256((size_t)g.BH * g.Mq * sizeof(int32_t));
+         align256((size_t)g.BH * g.Mq * sizeof(int32_t)) + align256(4 * sizeof(int32_t));
 }
 
 BwdWorkspace bwd_workspace_layout(const Geom& g, void* base) {
@@ -1062,6 +1178,8 @@ BwdWorkspace bwd_workspace_layout(const Geom& g, void* base) {
   w.col_order = reinterpret_cast<int32_t*>(p);
   p += align256((size_t)g.BH * g.Mk * sizeof(int32_t));
   w.row_order = reinterpret_cast<int32_t*>(p);
+  p += align256((size_t)g.BH * g.Mq * sizeof(int32_t));
+  w.work = reinterpret_cast<int32_t*>(p);
   return w;
 }
 

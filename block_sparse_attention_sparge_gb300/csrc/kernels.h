@@ -44,12 +44,14 @@ cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const v
                             float* lse, int32_t* status, cudaStream_t st);
 
 // attn_bwd.cu.  Workspace: D = rowsum(dO*O) fp32 [BH, N], then the
-// launch orders of kv-blocks [BH*Mk] and q-blocks [BH*Mq] (long lists first,
-// then index order).
+// launch orders of key tiles [<= BH*Mk] and q-blocks [BH*Mq] (long lists
+// first, then index order), then the work counters of the persistent
+// gradient kernels (int32 [4], zeroed by the first kernel of each call).
 struct BwdWorkspace {
   float* delta;
   int32_t* col_order;
   int32_t* row_order;
+  int32_t* work;
 };
 size_t bwd_workspace_bytes(const Geom& g);
 BwdWorkspace bwd_workspace_layout(const Geom& g, void* base);
