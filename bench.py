@@ -28,6 +28,7 @@ reference implementation of this method.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -332,14 +333,16 @@ def run_ours(args, wl, k_frac, p):
     def step(kf, pp, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        res = B.sparge_mask(q, k, kf, pp, out=mask_out, workspace=ws_mask)
+        res = B.sparge_mask(q, k, kf, pp, out=mask_out, workspace=ws_mask, block_kv=wl.block_kv)
         if ev is not None:
             ev[1].record(stream)
-        B.sparge_attn_fwd(q, k, v, res["row_idx"], res["row_cnt"], out=o, lse=lse, status=status)
+        B.sparge_attn_fwd(q, k, v, res["row_idx"], res["row_cnt"], out=o, lse=lse, status=status,
+                          block_kv=wl.block_kv)
         if ev is not None:
             ev[2].record(stream)
         B.sparge_attn_bwd(q, k, v, o, lse, do, res["row_idx"], res["row_cnt"], res["col_idx"],
-                          res["col_cnt"], out=(dq, dk, dv), workspace=ws_bwd, status=status)
+                          res["col_cnt"], out=(dq, dk, dv), workspace=ws_bwd, status=status,
+                          block_kv=wl.block_kv)
         if ev is not None:
             ev[3].record(stream)
         return res
@@ -451,11 +454,11 @@ def run_ours(args, wl, k_frac, p):
         alone = {}
         for name, mo in (("with_csc", mask_out), ("csr_only", mo_csr)):
             for _ in range(3):
-                B.sparge_mask(q, k, k_frac, p, out=mo, workspace=ws_mask)
+                B.sparge_mask(q, k, k_frac, p, out=mo, workspace=ws_mask, block_kv=wl.block_kv)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for _ in range(50):
-                B.sparge_mask(q, k, k_frac, p, out=mo, workspace=ws_mask)
+                B.sparge_mask(q, k, k_frac, p, out=mo, workspace=ws_mask, block_kv=wl.block_kv)
             e1.record(stream)
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / 50
@@ -490,18 +493,18 @@ def run_ours(args, wl, k_frac, p):
     # own rule k = 5 %, p = 0.9, whole step timed (the Top-p search included).
     local = None
     if not args.no_hybrid and wl.name == "wan480":
-        lwl = synth.WORKLOADS["wan480_local"]
+        lwl = dataclasses.replace(synth.WORKLOADS["wan480_local"], block_kv=wl.block_kv)
         lq, lk, lv, ldo = synth.video_inputs(lwl, device=dev)
         lo, llse = torch.empty_like(lq), torch.empty_like(lse)
         lg = tuple(torch.empty_like(lq) for _ in range(3))
 
         def lstep():
-            r = B.sparge_mask(lq, lk, lwl.k_frac, lwl.p, out=mask_out, workspace=ws_mask)
+            r = B.sparge_mask(lq, lk, lwl.k_frac, lwl.p, out=mask_out, workspace=ws_mask, block_kv=wl.block_kv)
             B.sparge_attn_fwd(lq, lk, lv, r["row_idx"], r["row_cnt"], out=lo, lse=llse,
-                              status=status)
+                              status=status, block_kv=wl.block_kv)
             B.sparge_attn_bwd(lq, lk, lv, lo, llse, ldo, r["row_idx"], r["row_cnt"],
                               r["col_idx"], r["col_cnt"], out=lg, workspace=ws_bwd,
-                              status=status)
+                              status=status, block_kv=wl.block_kv)
         lstep()
         torch.cuda.synchronize()
         mb = unpack_bits(mask_out["bitmask"], mk)
@@ -550,12 +553,12 @@ def run_ours(args, wl, k_frac, p):
 
         def compute(sl):
             qq, kk, vv, dd = sl["in"]
-            res = B.sparge_mask(qq, kk, k_frac, p, out=mask_out, workspace=ws_mask)
+            res = B.sparge_mask(qq, kk, k_frac, p, out=mask_out, workspace=ws_mask, block_kv=wl.block_kv)
             B.sparge_attn_fwd(qq, kk, vv, res["row_idx"], res["row_cnt"], out=sl["o"],
-                              lse=sl["lse"], status=status)
+                              lse=sl["lse"], status=status, block_kv=wl.block_kv)
             B.sparge_attn_bwd(qq, kk, vv, sl["o"], sl["lse"], dd, res["row_idx"],
                               res["row_cnt"], res["col_idx"], res["col_cnt"], out=sl["g"],
-                              workspace=ws_bwd, status=status)
+                              workspace=ws_bwd, status=status, block_kv=wl.block_kv)
 
         def pipelined(n, e_first=None, e_last=None):
             ev_in = [torch.cuda.Event() for _ in range(n)]
@@ -676,15 +679,16 @@ def run_sweep(args, wl):
         q, k, v, _ = gen(wl, device=dev)
         for kf in SWEEP_K:
             for pp in SWEEP_P:
-                res = B.sparge_mask(q, k, kf, pp, out=mask_out, workspace=ws_mask)
+                res = B.sparge_mask(q, k, kf, pp, out=mask_out, workspace=ws_mask, block_kv=wl.block_kv)
                 torch.cuda.synchronize()
                 maskb = unpack_bits(mask_out["bitmask"], mk)
                 pairs = kept_pairs(maskb, N, wl.block_q, wl.block_kv)
                 sparsity = 1.0 - float(maskb.sum().item()) / float(Bn * H * mq * mk)
                 t_mask = timed(lambda: B.sparge_mask(q, k, kf, pp, out=mask_out,
-                                                     workspace=ws_mask))
+                                                     workspace=ws_mask, block_kv=wl.block_kv))
                 t_fwd = timed(lambda: B.sparge_attn_fwd(q, k, v, res["row_idx"], res["row_cnt"],
-                                                        out=o, lse=lse, status=status))
+                                                        out=o, lse=lse, status=status,
+                                                        block_kv=wl.block_kv))
                 fl = 4.0 * d * pairs
                 cells.append({"rows": kind, "k_frac": kf, "p": pp, "sparsity": round(sparsity, 5),
                               "mask_ms": round(t_mask, 4),
@@ -717,6 +721,8 @@ def main(argv=None):
                     choices=("wan480", "wan720", "wan480_d64", "wan480_local"))
     ap.add_argument("--k-frac", type=float, default=None)
     ap.add_argument("--p", type=float, default=0.0, help="Top-p of the headline step (0 = off)")
+    ap.add_argument("--block-kv", type=int, default=None, choices=(64, 128),
+                    help="kv-block size (default: the workload's, 64)")
     ap.add_argument("--no-hybrid", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -728,6 +734,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     from block_sparse_attention_sparge_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
+    if args.block_kv is not None:
+        wl = dataclasses.replace(wl, block_kv=args.block_kv)
     k_frac = wl.k_frac if args.k_frac is None else args.k_frac
     if args.impl == "reference":
         return run_reference(args, wl, k_frac, args.p)

@@ -241,11 +241,12 @@ def sparge_mask_from_prob(prob: torch.Tensor, k_frac: float, p: float, N: int, d
 
 
 def sparge_attn_fwd(q, k, v, row_idx, row_cnt, softmax_scale: float = 0.0, check_status=False,
-                    out=None, lse=None, status=None):
-    """Block-sparse attention forward; returns (O bf16, LSE fp32)."""
+                    out=None, lse=None, status=None, block_kv=BLOCK_KV):
+    """Block-sparse attention forward; returns (O bf16, LSE fp32).  The lists
+    index kv-blocks of ``block_kv`` tokens (64 or 128)."""
     _need_cuda_bf16(q, k, v)
     lib = load_library()
-    shp = _shape(q)
+    shp = _shape(q, BLOCK_Q, block_kv)
     B, H, N, d = q.shape
     o = out if out is not None else torch.empty_like(q)
     lse = lse if lse is not None else torch.empty((B, H, N), dtype=torch.float32, device=q.device)
@@ -259,11 +260,11 @@ def sparge_attn_fwd(q, k, v, row_idx, row_cnt, softmax_scale: float = 0.0, check
 
 def sparge_attn_bwd(q, k, v, o, lse, dout, row_idx, row_cnt, col_idx, col_cnt,
                     softmax_scale: float = 0.0, check_status=False, workspace=None, out=None,
-                    status=None):
+                    status=None, block_kv=BLOCK_KV):
     """Gradients (dQ, dK, dV) of the block-sparse attention, mask held fixed."""
     _need_cuda_bf16(q, k, v, o, dout)
     lib = load_library()
-    shp = _shape(q)
+    shp = _shape(q, BLOCK_Q, block_kv)
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     else:

@@ -41,7 +41,7 @@ int check_shape(const sparge_shape* s) {
     return SPARGE_ERR_INVALID_ARG;
   if ((long long)s->B * s->H > 65535LL * 1024LL) return SPARGE_ERR_INVALID_ARG;
   if (s->d != 64 && s->d != 128) return SPARGE_ERR_UNSUPPORTED;
-  if (s->block_q != 128 || s->block_kv != 64) return SPARGE_ERR_UNSUPPORTED;
+  if (s->block_q != 128 || (s->block_kv != 64 && s->block_kv != 128)) return SPARGE_ERR_UNSUPPORTED;
   if (s->N > kMaxN) return SPARGE_ERR_UNSUPPORTED;
   return SPARGE_OK;
 }

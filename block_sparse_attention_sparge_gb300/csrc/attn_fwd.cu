@@ -8,7 +8,8 @@
 // its q-block's kept kv-blocks only.
 //
 // One CTA computes one 128-token q-block of one head, looping over its CSR
-// list of kept 64-token kv-blocks; two CTAs share an SM so that one CTA's
+// list of kept kv-blocks in steps of 64 keys (a 128-key block is two steps);
+// two CTAs share an SM so that one CTA's
 // latencies (barrier hand-offs, loads, its prologue and epilogue) overlap the
 // other's work.  Warp roles (224 threads):
 //   warp 4   TMA producer: Q once, then K_j / V_j into a 2-stage ring; a
@@ -101,7 +102,8 @@ template <int D>
 __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ row_idx,
-                    const int32_t* __restrict__ row_cnt, int N, int Mq, int Mk, float scale_log2,
+                    const int32_t* __restrict__ row_cnt, int N, int Mq, int Mk, int bk,
+                    float scale_log2,
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                     int32_t* __restrict__ status) {
   using C = FwdCfg<D>;
@@ -117,8 +119,15 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
   const int bh = blockIdx.x / Mq;
   const int qb = blockIdx.x % Mq;
   const long long row_id = (long long)bh * Mq + qb;
-  const int n = min(max(__ldg(row_cnt + row_id), 0), Mk);
+  const int nkv = min(max(__ldg(row_cnt + row_id), 0), Mk);
   const int32_t* list = row_idx + row_id * Mk;
+  // Steps of 64 keys: one per kept block of 64 keys, two per kept block of
+  // 128 (its halves).  First key row of step t:
+  const int sub = bk / kBN;
+  const int n = nkv * sub;
+  auto row_of = [&](int t) -> int {
+    return min(max(__ldg(list + t / sub), 0), Mk - 1) * bk + (t % sub) * kBN;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
@@ -154,11 +163,11 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
           report_error(status, SPARGE_ERR_TIMEOUT);
           break;
         }
-        const int j = min(max(__ldg(list + t), 0), Mk - 1);
+        const int rw = row_of(t);
         mbar_arrive_expect_tx(bar(C::B_KF + s), C::kKV);
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(s0 + C::off_k + s * C::kKV + c * kBN * 128, &tmK, bar(C::B_KF + s), c * 64,
-                      j * kBN, bh);
+                      rw, bh);
         if (t >= C::NST && !mbar_wait(bar(C::B_VE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
           report_error(status, SPARGE_ERR_TIMEOUT);
           break;
@@ -166,7 +175,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
         mbar_arrive_expect_tx(bar(C::B_VF + s), C::kKV);
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(s0 + C::off_v + s * C::kKV + c * kBN * 128, &tmV, bar(C::B_VF + s), c * 64,
-                      j * kBN, bh);
+                      rw, bh);
         issued = t + 1;
       }
       // Let the last loads land before the CTA can exit (they complete on their own).
@@ -247,10 +256,10 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
     const bool pos = scale_log2 > 0.f;
     const float masked = pos ? -INFINITY : INFINITY;
     // The kv-block index of the next tile is loaded one tile ahead.
-    int j_next = n > 0 ? min(max(__ldg(list), 0), Mk - 1) : 0;
+    int rw_next = n > 0 ? row_of(0) : 0;
     for (int t = 0; t < n; ++t) {
-      const int j = j_next;
-      if (t + 1 < n) j_next = min(max(__ldg(list + t + 1), 0), Mk - 1);
+      const int rw = rw_next;
+      if (t + 1 < n) rw_next = row_of(t + 1);
       if (!warp_wait(bar(C::B_SF + (t & 1)), (t >> 1) & 1)) {
         ok = false;
         break;
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
           x[48 + c] = __uint_as_float(rd[c]);
         }
       }
-      const int valid = N - j * kBN;
+      const int valid = N - rw;
       if (valid < kBN) {
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
@@ -415,7 +424,7 @@ cudaError_t launch_fwd_impl(const Geom& g, const void* q, const void* k, const v
   const float scale_log2 = scale * 1.4426950408889634f;
   const unsigned grid = static_cast<unsigned>((long long)g.BH * g.Mq);
   attn_fwd_kernel<D><<<grid, kFwdThreads, C::smem_alloc, st>>>(
-      tq, tk, tv, row_idx, row_cnt, g.N, g.Mq, g.Mk, scale_log2,
+      tq, tk, tv, row_idx, row_cnt, g.N, g.Mq, g.Mk, g.bk, scale_log2,
       static_cast<__nv_bfloat16*>(o), lse, status);
   return cudaGetLastError();
 }

@@ -51,8 +51,9 @@ enum sparge_status {
   SPARGE_ERR_TIMEOUT = -6      /* a device-side bounded wait gave up        */
 };
 
-/* Problem shape.  Supported: d in {64, 128}; block_q = 128; block_kv = 64;
- * 1 <= N <= 524288 (so Mk <= 8192); B*H >= 1. */
+/* Problem shape.  Supported: d in {64, 128}; block_q = 128; block_kv in
+ * {64, 128}; 1 <= N <= 524288 (so Mk <= 8192); B*H >= 1.  The mask and the
+ * attention calls of one problem use the same block sizes. */
 typedef struct sparge_shape {
   int32_t B, H, N, d;
   int32_t block_q, block_kv;

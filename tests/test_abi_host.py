@@ -71,7 +71,8 @@ def test_workspace_sizes(lib):
 @pytest.mark.parametrize("shape,code", [
     ((1, 2, 1024, 96, 128, 64), B.SPARGE_ERR_UNSUPPORTED),
     ((1, 2, 1024, 128, 64, 64), B.SPARGE_ERR_UNSUPPORTED),
-    ((1, 2, 1024, 128, 128, 128), B.SPARGE_ERR_UNSUPPORTED),
+    ((1, 2, 1024, 128, 128, 256), B.SPARGE_ERR_UNSUPPORTED),
+    ((1, 2, 1024, 128, 128, 32), B.SPARGE_ERR_UNSUPPORTED),
     ((1, 2, 600000, 128, 128, 64), B.SPARGE_ERR_UNSUPPORTED),
     ((0, 2, 1024, 128, 128, 64), B.SPARGE_ERR_INVALID_ARG),
     ((1, 2, 0, 128, 128, 64), B.SPARGE_ERR_INVALID_ARG),
