@@ -53,49 +53,65 @@ constexpr unsigned kFull = 0xffffffffu;
 // ---------------------------------------------------------------- pooling
 constexpr int kPoolThreads = 256;
 
-// Mean of `rows` rows of one block (d = D bf16 values per row); thread
-// t < D returns channel t.  Thread i reads 16-byte chunk (i % CH) of rows
-// i / CH, + RG, ...; the partial sums meet in `red`.  The caller
-// synchronises before reusing `red`.
+constexpr int kPoolRows = 256;  // consecutive rows (tokens) one CTA reads
+
+// Issues this thread's loads of a run of 256 rows (up to `rows` valid; d = D
+// bf16 values per row): 16-byte chunk t % CH of rows t / CH + RG * i
+// (i < L), all issued before any is used, so a CTA keeps 64 KB (d = 128) in
+// flight.
 template <int D>
-__device__ __forceinline__ float pool_block(const __nv_bfloat16* __restrict__ src, int rows,
-                                            float (*red)[D]) {
-  constexpr int CH = D / 8;              // 16-byte chunks per row
-  constexpr int RG = kPoolThreads / CH;  // rows read concurrently
+__device__ __forceinline__ void pool_loads(const __nv_bfloat16* __restrict__ src, int rows,
+                                           uint4 (&v)[kPoolRows * D / 8 / kPoolThreads]) {
+  constexpr int CH = D / 8;               // 16-byte chunks per row
+  constexpr int RG = kPoolThreads / CH;   // rows read concurrently
+  constexpr int L = kPoolRows / RG;       // loads per thread
   const int c = threadIdx.x % CH;
   const int rg = threadIdx.x / CH;
-  float acc[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  // Up to 128 rows / RG rows per thread; the loads are independent, so the
-  // unrolled loop keeps all of them in flight.
-#pragma unroll 8
-  for (int r = rg; r < rows; r += RG) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * D) + c);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+  for (int i = 0; i < L; ++i) {
+    const int r = rg + RG * i;
+    v[i] = r < rows ? __ldg(reinterpret_cast<const uint4*>(src + (long long)r * D) + c)
+                    : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Adds the loaded values into per-block partial sums: load i belongs to block
+// i * RG / BLK of the run; the sums go to red[row group][block][feature].
+template <int D, int BLK>
+__device__ __forceinline__ void pool_accumulate(const uint4 (&v)[kPoolRows * D / 8 / kPoolThreads],
+                                                float (*red)[4][D]) {
+  constexpr int CH = D / 8;
+  constexpr int RG = kPoolThreads / CH;
+  constexpr int L = kPoolRows / RG;
+  constexpr int G = kPoolRows / BLK;
+  float acc[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+#pragma unroll
+  for (int i = 0; i < L; ++i) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 f = __bfloat1622float2(h[e]);
-      acc[2 * e] += f.x;
-      acc[2 * e + 1] += f.y;
+      acc[i * RG / BLK][2 * e] += f.x;
+      acc[i * RG / BLK][2 * e + 1] += f.y;
     }
   }
+  const int c = threadIdx.x % CH, rg = threadIdx.x / CH;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) red[rg][c * 8 + e] = acc[e];
-  __syncthreads();
-  float s = 0.f;
-  if (threadIdx.x < D) {
+  for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int g = 0; g < RG; ++g) s += red[g][threadIdx.x];
-  }
-  return s / static_cast<float>(rows);
+    for (int e = 0; e < 8; ++e) red[rg][g][c * 8 + e] = acc[g][e];
 }
 
-// One CTA per (head, block) unit.  Units [0, BH*Mq) are Q blocks (when
-// do_q), the rest K blocks.  The means are row-major [BH, M, d]: fp32 into
-// qbar / kbar, or, when qhi is set, as the bf16 pair hi = bf16(mean),
-// lo = bf16(mean - hi) into qhi / qlo and khi / klo (the operands of the
-// pooled-logit MMAs, hi*hi + hi*lo + lo*hi).
+// One CTA per unit: 256 consecutive tokens of one head, i.e. 256 / block
+// size blocks.  Units [0, BH*UQ) cover the Q blocks (when do_q), the rest
+// the K blocks.  The means are row-major [BH, M, d]: fp32 into qbar / kbar,
+// or, when qhi is set, as the bf16 pair hi = bf16(mean), lo = bf16(mean - hi)
+// into qhi / qlo and khi / klo (the operands of the pooled-logit MMAs,
+// hi*hi + hi*lo + lo*hi).
 template <int D>
 __global__ void __launch_bounds__(kPoolThreads) pool_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int BH, int N,
@@ -105,37 +121,56 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(
   // Lets a kernel launched with programmatic serialization start early; it
   // waits for this grid's results itself.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ float red[kPoolThreads / (D / 8)][D];
+  constexpr int CH = D / 8;
+  constexpr int RG = kPoolThreads / CH;
+  __shared__ float red[RG][4][D];
+  const int UQ = (N + kPoolRows - 1) / kPoolRows;  // units per head, either tensor
   const long long unit = blockIdx.x;
-  const long long nq = do_q ? (long long)BH * Mq : 0;
+  const long long nq = do_q ? (long long)BH * UQ : 0;
   const bool is_q = unit < nq;
   const long long u = is_q ? unit : unit - nq;
   const int M = is_q ? Mq : Mk;
   const int blk = is_q ? bq : bk;
-  const int bh = static_cast<int>(u / M);
-  const int i = static_cast<int>(u % M);
-  const int r0 = i * blk;
+  const int G = kPoolRows / blk;
+  const int bh = static_cast<int>(u / UQ);
+  const int r0 = static_cast<int>(u % UQ) * kPoolRows;
   const __nv_bfloat16* src = (is_q ? q : k) + ((long long)bh * N + r0) * D;
-  const int rows = min(blk, N - r0);
-  const float mean = pool_block<D>(src, rows, red);
-  if (threadIdx.x < D) {
-    const long long o = ((long long)bh * M + i) * D + threadIdx.x;
+  const int rows = min(kPoolRows, N - r0);
+  uint4 v[kPoolRows * D / 8 / kPoolThreads];
+  pool_loads<D>(src, rows, v);
+  if (blk == 128)
+    pool_accumulate<D, 128>(v, red);
+  else
+    pool_accumulate<D, 64>(v, red);
+  __syncthreads();
+  for (int o = threadIdx.x; o < G * D; o += kPoolThreads) {
+    const int g = o / D, f = o % D;
+    const int i = r0 / blk + g;  // block index within the head
+    if (i >= M) continue;
+    float sum = 0.f;
+#pragma unroll
+    for (int x = 0; x < RG; ++x) sum += red[x][g][f];
+    const float mean = sum / static_cast<float>(min(blk, N - i * blk));
+    const long long oi = ((long long)bh * M + i) * D + f;
     if (qhi != nullptr) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(mean);
-      const __nv_bfloat16 l = __float2bfloat16_rn(mean - __bfloat162float(h));
-      (is_q ? qhi : khi)[o] = h;
-      (is_q ? qlo : klo)[o] = l;
+      const __nv_bfloat16 hh = __float2bfloat16_rn(mean);
+      const __nv_bfloat16 ll = __float2bfloat16_rn(mean - __bfloat162float(hh));
+      (is_q ? qhi : khi)[oi] = hh;
+      (is_q ? qlo : klo)[oi] = ll;
     } else {
-      (is_q ? qbar : kbar)[o] = mean;
+      (is_q ? qbar : kbar)[oi] = mean;
     }
   }
 }
 
-// One CTA per unit (units = the Q and K blocks to pool).
+// One CTA per unit of 256 tokens (units = the Q and K runs to pool).
 template <int D>
-cudaError_t launch_pool_kernel(const Geom& g, const void* q, const void* k, int do_q,
-                               long long units, float* qbar, float* kbar, void* qhi, void* qlo,
-                               void* khi, void* klo, cudaStream_t st) {
+cudaError_t launch_pool_kernel(const Geom& g, const void* q, const void* k, int do_q, int do_k,
+                               float* qbar, float* kbar, void* qhi, void* qlo, void* khi,
+                               void* klo, cudaStream_t st) {
+  const long long uq = (g.N + kPoolRows - 1) / kPoolRows;
+  const long long units = (do_q ? (long long)g.BH * uq : 0) + (do_k ? (long long)g.BH * uq : 0);
+  if (units == 0) return cudaSuccess;
   pool_kernel<D><<<static_cast<unsigned>(units), kPoolThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g.BH, g.N, g.bq,
       g.bk, g.Mq, g.Mk, do_q, qbar, kbar, static_cast<__nv_bfloat16*>(qhi),
@@ -893,12 +928,10 @@ cudaError_t launch_pool(const Geom& g, const void* q, const void* k, float* qbar
                         cudaStream_t st) {
   const int do_q = qbar != nullptr;
   const int do_k = kbar != nullptr;
-  const long long units = (do_q ? (long long)g.BH * g.Mq : 0) + (do_k ? (long long)g.BH * g.Mk : 0);
-  if (units == 0) return cudaSuccess;
   if (g.d == 128)
-    return launch_pool_kernel<128>(g, q, k, do_q, units, qbar, kbar, nullptr, nullptr, nullptr,
+    return launch_pool_kernel<128>(g, q, k, do_q, do_k, qbar, kbar, nullptr, nullptr, nullptr,
                                    nullptr, st);
-  return launch_pool_kernel<64>(g, q, k, do_q, units, qbar, kbar, nullptr, nullptr, nullptr,
+  return launch_pool_kernel<64>(g, q, k, do_q, do_k, qbar, kbar, nullptr, nullptr, nullptr,
                                 nullptr, st);
 }
 
@@ -954,8 +987,7 @@ cudaError_t launch_mask_pipeline_impl(const Geom& g, const void* q, const void* 
       make_tmap_bf16(&tkh, khi, g.BH, g.Mk, D, kLgTile) != 0 ||
       make_tmap_bf16(&tkl, klo, g.BH, g.Mk, D, kLgTile) != 0)
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_pool_kernel<D>(g, q, k, 1, (long long)g.BH * (g.Mq + g.Mk), nullptr,
-                                        nullptr, qhi, qlo, khi, klo, st);
+  cudaError_t e = launch_pool_kernel<D>(g, q, k, 1, 1, nullptr, nullptr, qhi, qlo, khi, klo, st);
   if (e != cudaSuccess) return e;
   using L = LgCfg<D>;
   const int nmt = (g.Mq + kLgTile - 1) / kLgTile, nnt = (g.Mk + kLgTile - 1) / kLgTile;
