@@ -202,6 +202,7 @@ struct DkdvCfg {
   // Q and dO arrive per 64-query half of a q-block: a slot holds Q_h and dO_h
   // (64 rows each) and is released once the gradient MMAs of that half are done.
   static constexpr int NSLOT = D == 128 ? 4 : 8;
+  static constexpr int NRING = 4;                    // key tiles handed out ahead
   static constexpr uint32_t kKP = kPair * D * 2;     // K (or V) of the 128 keys
   static constexpr uint32_t kQh = 64 * D * 2;        // one Q (or dO) half tile
   static constexpr uint32_t kChunkK = kPair * 128;   // 64-column chunk of the key tile
@@ -212,19 +213,24 @@ struct DkdvCfg {
   static constexpr uint32_t off_do = off_q + NSLOT * kQh;      // NSLOT dO halves
   static constexpr uint32_t off_row = off_do + NSLOT * kQh;    // NSLOT x {lse*log2e [64], D [64]}
   static constexpr uint32_t off_info = off_row + NSLOT * 2 * 64 * 4;  // NSLOT x int32
-  static constexpr uint32_t off_bar = off_info + 64;
-  static constexpr int B_KV = 0;
-  static constexpr int B_QF = 1;              // NSLOT, count 32 (producer lanes) + tx
+  static constexpr uint32_t off_ring = off_info + 64;          // NRING x {tile, entries}
+  static constexpr uint32_t off_bar = off_ring + 64;
+  static constexpr int B_KV = 0;              // K/V of a key tile landed
+  static constexpr int B_KVE = 1;             // its S^T and dP^T MMAs done: K/V slots free
+  static constexpr int B_QF = 2;              // NSLOT, count 32 (producer lanes) + tx
   static constexpr int B_QE = B_QF + NSLOT;   // NSLOT: the half's gradient MMAs done
   // Per query half h, S^T and dP^T are tracked separately, so that P^T and
   // dV of a half proceed while dP^T and dS^T of it are still in flight.
   static constexpr int B_SSF = B_QE + NSLOT;  // 2: S^T_h in TMEM
   static constexpr int B_DPF = B_SSF + 2;     // 2: dP^T_h in TMEM
-  static constexpr int B_PPF = B_DPF + 2;     // 2, count 256: P^T_h written
-  static constexpr int B_DSF = B_PPF + 2;     // 2, count 256: dS^T_h written
+  static constexpr int B_PPF = B_DPF + 2;     // 2, all compute threads: P^T_h written
+  static constexpr int B_DSF = B_PPF + 2;     // 2, all compute threads: dS^T_h written
   static constexpr int B_RVF = B_DSF + 2;     // 2: dV MMAs of half h done (S^T_h region free)
   static constexpr int B_RKF = B_RVF + 2;     // 2: dK MMAs of half h done (dP^T_h region free)
-  static constexpr int B_DONE = B_RKF + 2;    // count 2
+  static constexpr int B_DKE = B_RKF + 2;     // all compute threads: dV, dK read out
+  static constexpr int B_IF = B_DKE + 1;      // NRING: key tile handed out
+  static constexpr int B_IE = B_IF + NRING;   // NRING: read by both issuers and every compute warp
+  static constexpr int B_DONE = B_IE + NRING; // count 2
   static constexpr int NBAR = B_DONE + 1;
   static constexpr uint32_t off_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_slot + 16;
@@ -240,20 +246,25 @@ struct DkdvCfg {
   static constexpr uint32_t col_dk = 384;
 };
 
-// One CTA per key tile: 128 keys = the 64-key kv-blocks j0 = 2 * jt and
-// j1 = 2 * jt + 1 (kv_per_tile = 2), or the one 128-key block jt
-// (kv_per_tile = 1; then both 64-row halves belong to it).
+// Persistent: one CTA per SM takes key tiles from a work counter in the
+// launch order (long column lists first).  A key tile is 128 keys: the 64-key
+// kv-blocks j0 = 2 * jt and j1 = 2 * jt + 1 (kv_per_tile = 2), or the one
+// 128-key block jt (kv_per_tile = 1; then both 64-row halves belong to it).
+// The entries of successive tiles share one running entry count t, which
+// indexes the Q/dO slot ring and the barrier phases; the next tile's K/V
+// load, S^T and P^T overlap the current tile's last entries and epilogue.
 template <int D>
 __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const float* __restrict__ lse, const float* __restrict__ delta,
                     const int32_t* __restrict__ col_idx, const int32_t* __restrict__ col_cnt,
-                    const int32_t* __restrict__ tile_order, int N, int Mq, int Mk, int Mt,
-                    int kv_per_tile, float scale, float scale_log2,
+                    const int32_t* __restrict__ tile_order, int ntiles, int32_t* __restrict__ work,
+                    int N, int Mq, int Mk, int Mt, int kv_per_tile, float scale, float scale_log2,
                     __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
                     int32_t* __restrict__ status) {
   using C = DkdvCfg<D>;
+  using R = Roles<kDkdvWarps>;
   // The dQ kernel (independent of this one) may start on SMs this grid's
   // last CTAs leave idle.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -264,50 +275,24 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
   int32_t* info = reinterpret_cast<int32_t*>(sm + C::off_info);
+  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(sm + C::off_ring);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = min(max(__ldg(tile_order + blockIdx.x), 0), static_cast<int>(gridDim.x) - 1);
-  const int bh = item / Mt;
-  const int jt = item % Mt;
-  const int key0 = jt * kPair;  // first key token of the tile
-
-  // The two column lists (one list, taken for both halves, for a 128-key block).
   const bool paired = kv_per_tile == 2;
-  const int ja = paired ? 2 * jt : jt;
-  const int jb = paired ? 2 * jt + 1 : jt;
-  const int32_t* list0 = col_idx + ((long long)bh * Mk + ja) * Mq;
-  const int32_t* list1 = col_idx + ((long long)bh * Mk + min(jb, Mk - 1)) * Mq;
-  const int n0 = min(max(__ldg(col_cnt + (long long)bh * Mk + ja), 0), Mq);
-  const int n1 = (paired && jb < Mk) ? min(max(__ldg(col_cnt + (long long)bh * Mk + jb), 0), Mq) : 0;
 
-  // Length of the union of the two ascending lists: n0 + n1 minus the common
-  // entries, counted by binary search of list0's entries in list1.
-  if (threadIdx.x == 0) slot[1] = 0;
-  __syncthreads();
-  if (paired) {
-    int common = 0;
-    for (int e = threadIdx.x; e < n0; e += Roles<kDkdvWarps>::kThreads) {
-      const int x = __ldg(list0 + e);
-      int lo = 0, hi = n1;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(list1 + mid) < x) lo = mid + 1; else hi = mid;
-      }
-      common += (lo < n1 && __ldg(list1 + lo) == x) ? 1 : 0;
-    }
-    if (common) atomicAdd(reinterpret_cast<int*>(slot + 1), common);
-  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
       if (i >= C::B_QF && i < C::B_QF + C::NSLOT) cnt = 32;
-      if (i >= C::B_PPF && i < C::B_PPF + 4) cnt = 32 * Roles<kDkdvWarps>::kCompute;  // PPF, DSF
+      if (i >= C::B_PPF && i < C::B_PPF + 4) cnt = 32 * R::kCompute;  // PPF, DSF
+      if (i == C::B_DKE) cnt = 32 * R::kCompute;
+      if (i >= C::B_IE && i < C::B_IE + C::NRING) cnt = 2 + R::kCompute;
       if (i == C::B_DONE) cnt = 2;
       mbar_init(bar(i), cnt);
     }
     fence_barrier_init();
   }
-  if (warp == Roles<kDkdvWarps>::kIssueA) {
+  if (warp == R::kIssueA) {
     tmem_alloc(smem_u32(slot), C::tmem_cols);
     tmem_relinquish();
   }
@@ -315,29 +300,105 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = slot[0];
-  const int n = paired ? n0 + n1 - static_cast<int>(slot[1]) : n0;
 
-  if (warp == Roles<kDkdvWarps>::kProducer) {
+  // The seq-th key tile of this CTA and its entry count, as handed out by the
+  // producer through the ring (tile -1: no more work, -2: the producer gave up).
+  auto next_tile = [&](int seq, bool ok, int* n) -> int {
+    const int rs = seq % C::NRING;
+    if (!ok || !mbar_wait(bar(C::B_IF + rs), (seq / C::NRING) & 1, kWaitTimeoutNs)) return -2;
+    *n = ring[2 * rs + 1];
+    return ring[2 * rs];
+  };
+  auto release_tile = [&](int seq) { mbar_arrive(bar(C::B_IE + seq % C::NRING)); };
+  struct Tile {
+    int bh, jt, key0, n0, n1;
+    const int32_t *list0, *list1;
+  };
+  auto tile_info = [&](int it) -> Tile {
+    Tile x;
+    x.bh = it / Mt;
+    x.jt = it % Mt;
+    x.key0 = x.jt * kPair;
+    const int ja = paired ? 2 * x.jt : x.jt;
+    const int jb = paired ? 2 * x.jt + 1 : x.jt;
+    x.list0 = col_idx + ((long long)x.bh * Mk + ja) * Mq;
+    x.list1 = col_idx + ((long long)x.bh * Mk + min(jb, Mk - 1)) * Mq;
+    x.n0 = min(max(__ldg(col_cnt + (long long)x.bh * Mk + ja), 0), Mq);
+    x.n1 = (paired && jb < Mk) ? min(max(__ldg(col_cnt + (long long)x.bh * Mk + jb), 0), Mq) : 0;
+    return x;
+  };
+
+  if (warp == R::kProducer) {
     // ---------------------------------------------------------- producer
-    if (n > 0) {
+    // All 32 lanes: they count the union of a tile's two ascending column
+    // lists (list0's entries searched in list1) and load the rows' lse and D;
+    // lane 0 issues the TMA copies.
+    int t = 0, j = 0;  // running entry count; tiles with work so far
+    bool ok = true;
+    for (int seq = 0;; ++seq) {
+      const int rs = seq % C::NRING;
+      if (seq >= C::NRING &&
+          !mbar_wait(bar(C::B_IE + rs), ((seq / C::NRING) - 1) & 1, kWaitTimeoutNs))
+        ok = false;
+      ok = __all_sync(0xffffffffu, ok);
+      int it = -1;
+      if (ok) {
+        int k = 0;
+        if (lane == 0) k = atomicAdd(work, 1);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        it = k < ntiles ? min(max(__ldg(tile_order + k), 0), ntiles - 1) : -1;
+      }
+      Tile x{};
+      int n = 0;
+      if (it >= 0) {
+        x = tile_info(it);
+        int common = 0;
+        if (paired) {
+          for (int e = lane; e < x.n0; e += 32) {
+            const int v = __ldg(x.list0 + e);
+            int lo = 0, hi = x.n1;
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (__ldg(x.list1 + mid) < v) lo = mid + 1; else hi = mid;
+            }
+            common += (lo < x.n1 && __ldg(x.list1 + lo) == v) ? 1 : 0;
+          }
+          common = __reduce_add_sync(0xffffffffu, common);
+        }
+        n = paired ? x.n0 + x.n1 - common : x.n0;
+      }
+      if (lane == 0) {
+        ring[2 * rs] = ok ? it : -2;
+        ring[2 * rs + 1] = n;
+        mbar_arrive(bar(C::B_IF + rs));
+      }
+      if (it < 0) break;
+      if (n == 0) continue;
+      if (j >= 1 && !mbar_wait(bar(C::B_KVE), (j - 1) & 1, kWaitTimeoutNs)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        continue;  // publishes the failure in the next ring slot, then stops
+      }
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::kKP);
         for (int c = 0; c < D / 64; ++c) {
           const uint32_t o = c * C::kChunkK;
-          tma_load_3d(s0 + C::off_k + o, &tmK, bar(C::B_KV), c * 64, key0, bh);
-          tma_load_3d(s0 + C::off_k + o + kBN * 128, &tmK, bar(C::B_KV), c * 64, key0 + kBN, bh);
-          tma_load_3d(s0 + C::off_v + o, &tmV, bar(C::B_KV), c * 64, key0, bh);
-          tma_load_3d(s0 + C::off_v + o + kBN * 128, &tmV, bar(C::B_KV), c * 64, key0 + kBN, bh);
+          tma_load_3d(s0 + C::off_k + o, &tmK, bar(C::B_KV), c * 64, x.key0, x.bh);
+          tma_load_3d(s0 + C::off_k + o + kBN * 128, &tmK, bar(C::B_KV), c * 64, x.key0 + kBN,
+                      x.bh);
+          tma_load_3d(s0 + C::off_v + o, &tmV, bar(C::B_KV), c * 64, x.key0, x.bh);
+          tma_load_3d(s0 + C::off_v + o + kBN * 128, &tmV, bar(C::B_KV), c * 64, x.key0 + kBN,
+                      x.bh);
         }
       }
-      const float* lse_h = lse + (long long)bh * N;
-      const float* del_h = delta + (long long)bh * N;
-      int a = 0, b = 0, issued = 0;
-      bool ok = true;
-      for (int t = 0; ok && t < n; ++t) {
+      ++j;
+      const float* lse_h = lse + (long long)x.bh * N;
+      const float* del_h = delta + (long long)x.bh * N;
+      int a = 0, b = 0;
+      for (int e = 0; e < n; ++e, ++t) {
         // Next entry of the union (every lane walks the lists identically).
-        const int x0 = a < n0 ? min(max(__ldg(list0 + a), 0), Mq - 1) : Mq;
-        const int x1 = b < n1 ? min(max(__ldg(list1 + b), 0), Mq - 1) : Mq;
+        const int x0 = a < x.n0 ? min(max(__ldg(x.list0 + a), 0), Mq - 1) : Mq;
+        const int x1 = b < x.n1 ? min(max(__ldg(x.list1 + b), 0), Mq - 1) : Mq;
         const int i = min(x0, x1);
         int flags = paired ? ((x0 == i ? 1 : 0) | (x1 == i ? 2 : 0)) : 3;
         if (x0 == i) ++a;
@@ -351,7 +412,6 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
             ok = false;
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
-            report_error(status, SPARGE_ERR_TIMEOUT);
             break;
           }
           const int row0 = ic * kBM + h * 64;
@@ -359,9 +419,9 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
             mbar_expect_tx(bar(C::B_QF + sl), 2 * C::kQh);
             for (int c = 0; c < D / 64; ++c) {
               tma_load_3d(s0 + C::off_q + sl * C::kQh + c * C::kChunkH, &tmQ, bar(C::B_QF + sl),
-                          c * 64, row0, bh);
+                          c * 64, row0, x.bh);
               tma_load_3d(s0 + C::off_do + sl * C::kQh + c * C::kChunkH, &tmDO,
-                          bar(C::B_QF + sl), c * 64, row0, bh);
+                          bar(C::B_QF + sl), c * 64, row0, x.bh);
             }
             info[sl] = ic | (flags << 24);
           }
@@ -377,264 +437,321 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
           reinterpret_cast<float2*>(rowv)[lane] = l2;
           reinterpret_cast<float2*>(rowv + 64)[lane] = d2;
           mbar_arrive(bar(C::B_QF + sl));
-          issued = k + 1;
         }
-      }
-      // Let the last loads land before the CTA can exit.
-      if (lane == 0) {
-        mbar_wait(bar(C::B_KV), 0, kWaitTimeoutNs);
-        for (int k = max(0, issued - C::NSLOT); k < issued; ++k)
-          mbar_wait(bar(C::B_QF + k % C::NSLOT), (k / C::NSLOT) & 1, kWaitTimeoutNs);
+        if (!ok) break;
       }
     }
-  } else if (warp == Roles<kDkdvWarps>::kIssueA) {
+    if (!ok && lane == 0) report_error(status, SPARGE_ERR_TIMEOUT);
+    // Let the last loads land before the CTA can exit.
+    if (lane == 0) {
+      if (j > 0) mbar_wait(bar(C::B_KV), (j - 1) & 1, kWaitTimeoutNs);
+      for (int k = max(0, 2 * t - C::NSLOT); k < 2 * t; ++k)
+        mbar_wait(bar(C::B_QF + k % C::NSLOT), (k / C::NSLOT) & 1, kWaitTimeoutNs);
+    }
+  } else if (warp == R::kIssueA) {
     // ---------------------------------------------------------- S^T, dP^T
     // S^T_h = K Q_h^T and dP^T_h = V dO_h^T (M = 128 keys, N = 64 queries of
     // half h, K = d).
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kPair, 64, false, false);
       const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(s0 + C::off_v, 16, 1024);
-      bool ok = mbar_wait(bar(C::B_KV), 0, kWaitTimeoutNs);
-      for (int t = 0; ok && t < n; ++t) {
-        for (int h = 0; h < 2; ++h) {
-          const int k = 2 * t + h, sl = k % C::NSLOT;
-          // S^T_h's columns hold P^T_h of entry t - 1 until its dV MMAs are
-          // done, dP^T_h's hold dS^T_h until its dK MMAs are.
-          if (!mbar_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1, kWaitTimeoutNs) ||
-              (t >= 1 && !mbar_wait(bar(C::B_RVF + h), (t - 1) & 1, kWaitTimeoutNs))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, 16, 1024);
-          const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, 16, 1024);
-          const uint32_t dS = tmem + h * 128;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
-            const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
-            tc_mma_bf16(dS, sdesc_add(dk0, ka), sdesc_add(dq, kb), idS, kk > 0);
-          }
-          tc_commit(bar(C::B_SSF + h));
-          if (t >= 1 && !mbar_wait(bar(C::B_RKF + h), (t - 1) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
-            const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
-            tc_mma_bf16(dS + 64, sdesc_add(dv0, ka), sdesc_add(ddo, kb), idS, kk > 0);
-          }
-          tc_commit(bar(C::B_DPF + h));
+      bool ok = true;
+      int t = 0, j = 0;
+      for (int seq = 0;; ++seq) {
+        int n = 0;
+        const int it = next_tile(seq, ok, &n);
+        release_tile(seq);
+        if (it < 0) {
+          if (it == -2) ok = false;
+          break;
         }
+        if (n == 0) continue;
+        if (!mbar_wait(bar(C::B_KV), j & 1, kWaitTimeoutNs)) {
+          ok = false;
+          break;
+        }
+        ++j;
+        for (int e = 0; ok && e < n; ++e, ++t) {
+          for (int h = 0; h < 2; ++h) {
+            const int k = 2 * t + h, sl = k % C::NSLOT;
+            // S^T_h's columns hold P^T_h of entry t - 1 until its dV MMAs are
+            // done, dP^T_h's hold dS^T_h until its dK MMAs are.
+            if (!mbar_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1, kWaitTimeoutNs) ||
+                (t >= 1 && !mbar_wait(bar(C::B_RVF + h), (t - 1) & 1, kWaitTimeoutNs))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, 16, 1024);
+            const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, 16, 1024);
+            const uint32_t dS = tmem + h * 128;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+              const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
+              tc_mma_bf16(dS, sdesc_add(dk0, ka), sdesc_add(dq, kb), idS, kk > 0);
+            }
+            tc_commit(bar(C::B_SSF + h));
+            if (t >= 1 && !mbar_wait(bar(C::B_RKF + h), (t - 1) & 1, kWaitTimeoutNs)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+              const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
+              tc_mma_bf16(dS + 64, sdesc_add(dv0, ka), sdesc_add(ddo, kb), idS, kk > 0);
+            }
+            tc_commit(bar(C::B_DPF + h));
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar(C::B_KVE));  // every S^T and dP^T of this tile issued
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
-  } else if (warp == Roles<kDkdvWarps>::kIssueB) {
+  } else if (warp == R::kIssueB) {
     // ---------------------------------------------------------- dV, dK
     // dV += P^T_h dO_h and dK += dS^T_h Q_h (M = 128 keys, N = d, K = the 64
-    // queries of half h); A from TMEM, B = dO_h / Q_h read MN-major.
-    if (lane == 0 && n > 0) {
+    // queries of half h); A from TMEM, B = dO_h / Q_h read MN-major.  The
+    // first MMAs of a tile overwrite the accumulators, after the compute
+    // warps have read out the previous tile's.
+    if (lane == 0) {
       constexpr uint32_t idG = idesc_bf16(kPair, D, false, true);
+      constexpr int NC = 64 / (R::kCompute / 4);
       bool ok = true;
-      for (int t = 0; ok && t < n; ++t) {
-        for (int h = 0; h < 2; ++h) {
-          const int sl = (2 * t + h) % C::NSLOT;
-          const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, C::kChunkH, 1024);
-          const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, C::kChunkH, 1024);
-          const uint32_t ap = tmem + h * 128;
-          // Queries 16kk .. 16kk + 15 of the half: the TMEM columns where the
-          // compute warp group holding them wrote their bf16 pairs.
-          constexpr int NC = 64 / (Roles<kDkdvWarps>::kCompute / 4);
-          if (!mbar_wait(bar(C::B_PPF + h), t & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16_ta(tmem + C::col_dv, ap + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
-                           sdesc_add(ddo, kk * 2048), idG,
-                           (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(C::B_RVF + h));
-          if (!mbar_wait(bar(C::B_DSF + h), t & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16_ta(tmem + C::col_dk, ap + 64 + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
-                           sdesc_add(dq, kk * 2048), idG,
-                           (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(C::B_RKF + h));
-          tc_commit(bar(C::B_QE + sl));
+      int t = 0, j = 0;
+      for (int seq = 0;; ++seq) {
+        int n = 0;
+        const int it = next_tile(seq, ok, &n);
+        release_tile(seq);
+        if (it < 0) {
+          if (it == -2) ok = false;
+          break;
         }
+        if (n == 0) continue;
+        for (int e = 0; ok && e < n; ++e, ++t) {
+          for (int h = 0; h < 2; ++h) {
+            const int sl = (2 * t + h) % C::NSLOT;
+            const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, C::kChunkH, 1024);
+            const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, C::kChunkH, 1024);
+            const uint32_t ap = tmem + h * 128;
+            const bool first = e == 0 && h == 0;
+            if (!mbar_wait(bar(C::B_PPF + h), t & 1, kWaitTimeoutNs) ||
+                (first && j >= 1 && !mbar_wait(bar(C::B_DKE), (j - 1) & 1, kWaitTimeoutNs))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // Queries 16kk .. 16kk + 15 of the half: the TMEM columns where the
+            // compute warp group holding them wrote their bf16 pairs.
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_bf16_ta(tmem + C::col_dv, ap + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
+                             sdesc_add(ddo, kk * 2048), idG, (!first || kk > 0) ? 1u : 0u);
+            tc_commit(bar(C::B_RVF + h));
+            if (!mbar_wait(bar(C::B_DSF + h), t & 1, kWaitTimeoutNs)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_bf16_ta(tmem + C::col_dk, ap + 64 + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
+                             sdesc_add(dq, kk * 2048), idG, (!first || kk > 0) ? 1u : 0u);
+            tc_commit(bar(C::B_RKF + h));
+            tc_commit(bar(C::B_QE + sl));
+          }
+        }
+        ++j;
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
       tc_commit(bar(C::B_DONE));
       mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
     }
-  } else {
+  } else if (warp < R::kCompute) {
     // ---------------------------------------------------------- compute
     // Thread = key row r (TMEM lane).  All compute warps take half 0 of an
     // entry, then half 1; within a half, warp group g = warp / 4 takes the NC
     // queries NC*g .. NC*g + NC - 1.
-    constexpr int NC = 64 / (Roles<kDkdvWarps>::kCompute / 4);
+    constexpr int NC = 64 / (R::kCompute / 4);
+    constexpr int FPW = D / (R::kCompute / 4);  // features per warp in the epilogue
     const int quarter = warp & 3, cg = warp >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool key_in = key0 + r < N;
     const int flag_bit = r < kBN ? 1 : 2;  // warp-uniform (quarters 0-1 vs 2-3)
     bool ok = true;
-    for (int t = 0; ok && t < n; ++t) {
-      for (int h = 0; h < 2; ++h) {
-        const int k = 2 * t + h, sl = k % C::NSLOT;
-        if (!warp_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1) ||
-            !warp_wait(bar(C::B_SSF + h), t & 1)) {
-          ok = false;
-          break;
-        }
-        const int flags = info[sl] >> 24;
-        const bool live = (flags & flag_bit) != 0;  // warp-uniform
-        const float* rowv = reinterpret_cast<const float*>(sm + C::off_row + sl * (2 * 64 * 4));
-        tc_fence_after();
-        const uint32_t sa = lane_base + h * 128 + NC * cg;
-        // P^T first (from S^T alone); it is the A operand of dV.
-        float p[NC];
-        uint32_t pk[NC / 2];
-        if (live) {
-          uint32_t sr[NC / 16][16];
-#pragma unroll
-          for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 16 * c, sr[c]);
-#pragma unroll
-          for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(sr[c]);
-          const float4* l4 = reinterpret_cast<const float4*>(rowv + NC * cg);
-#pragma unroll
-          for (int g = 0; g < NC / 4; ++g) {
-            const float4 lv = l4[g];
-            const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = g * 4 + e;
-              p[col] = ex2_approx(fmaf(__uint_as_float(sr[col / 16][col % 16]), scale_log2, -lq[e]));
-            }
-          }
-          if (!key_in) {
-#pragma unroll
-            for (int e = 0; e < NC; ++e) p[e] = 0.f;
-          }
-#pragma unroll
-          for (int e = 0; e < NC / 2; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < NC; ++e) p[e] = 0.f;
-#pragma unroll
-          for (int e = 0; e < NC / 2; ++e) pk[e] = 0u;
-        }
-        // P^T over the first NC/2 of the NC S^T columns this thread read.
-        if constexpr (NC == 32) {
-          SPARGE_TMEM_ST_X16(sa, pk);
-        } else {
-          SPARGE_TMEM_ST_X8(sa, pk);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_PPF + h));
-        // dS^T = P^T * (dP^T - D).
-        if (!warp_wait(bar(C::B_DPF + h), t & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (live) {
-          uint32_t dr[NC / 16][16];
-#pragma unroll
-          for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 64 + 16 * c, dr[c]);
-#pragma unroll
-          for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(dr[c]);
-          const float4* d4 = reinterpret_cast<const float4*>(rowv + 64 + NC * cg);
-#pragma unroll
-          for (int g = 0; g < NC / 4; ++g) {
-            const float4 dv4 = d4[g];
-            const float dq4[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-            float ds[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = g * 4 + e;
-              ds[e] = p[col] * (__uint_as_float(dr[col / 16][col % 16]) - dq4[e]);
-            }
-            pk[g * 2 + 0] = pack_bf16x2(ds[0], ds[1]);
-            pk[g * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
-          }
-        }
-        if constexpr (NC == 32) {
-          SPARGE_TMEM_ST_X16(sa + 64, pk);
-        } else {
-          SPARGE_TMEM_ST_X8(sa + 64, pk);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_DSF + h));
+    int t = 0;
+    for (int seq = 0;; ++seq) {
+      int n = 0;
+      const int it = next_tile(seq, ok, &n);
+      __syncwarp();
+      if (lane == 0) release_tile(seq);
+      if (it < 0) {
+        if (it == -2) ok = false;
+        break;
       }
-    }
-    if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-    // Epilogue: lane r holds key r of dV and dK; warp group cg writes its
-    // share of the features.
-    bool have = ok && n > 0;
-    if (have) {
-      have = warp_wait(bar(C::B_RKF + 0), (n - 1) & 1) && warp_wait(bar(C::B_RKF + 1), (n - 1) & 1);
-      if (!have) report_error(status, SPARGE_ERR_TIMEOUT);
-    }
-    tc_fence_after();
-    const long long rowoff = ((long long)bh * N + key0 + r) * D;
+      const int bh = it / Mt, key0 = (it % Mt) * kPair;
+      const bool key_in = key0 + r < N;
+      const long long rowoff = ((long long)bh * N + key0 + r) * D;
+      if (n == 0) {
+        // Keys no q-block keeps: dK = dV = 0.
+        if (key_in) {
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          for (int cc = cg * FPW; cc < (cg + 1) * FPW; cc += 8) {
+            __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc), z);
+            __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc), z);
+          }
+        }
+        continue;
+      }
+      for (int e = 0; ok && e < n; ++e, ++t) {
+        for (int h = 0; h < 2; ++h) {
+          const int k = 2 * t + h, sl = k % C::NSLOT;
+          if (!warp_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1) ||
+              !warp_wait(bar(C::B_SSF + h), t & 1)) {
+            ok = false;
+            break;
+          }
+          const int flags = info[sl] >> 24;
+          const bool live = (flags & flag_bit) != 0;  // warp-uniform
+          const float* rowv = reinterpret_cast<const float*>(sm + C::off_row + sl * (2 * 64 * 4));
+          tc_fence_after();
+          const uint32_t sa = lane_base + h * 128 + NC * cg;
+          // P^T first (from S^T alone); it is the A operand of dV.
+          float p[NC];
+          uint32_t pk[NC / 2];
+          if (live) {
+            uint32_t sr[NC / 16][16];
+#pragma unroll
+            for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 16 * c, sr[c]);
+#pragma unroll
+            for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(sr[c]);
+            const float4* l4 = reinterpret_cast<const float4*>(rowv + NC * cg);
+#pragma unroll
+            for (int g = 0; g < NC / 4; ++g) {
+              const float4 lv = l4[g];
+              const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const int col = g * 4 + q4;
+                p[col] = ex2_approx(fmaf(__uint_as_float(sr[col / 16][col % 16]), scale_log2,
+                                         -lq[q4]));
+              }
+            }
+            if (!key_in) {
+#pragma unroll
+              for (int q4 = 0; q4 < NC; ++q4) p[q4] = 0.f;
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < NC / 2; ++q4) pk[q4] = pack_bf16x2(p[2 * q4], p[2 * q4 + 1]);
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < NC; ++q4) p[q4] = 0.f;
+#pragma unroll
+            for (int q4 = 0; q4 < NC / 2; ++q4) pk[q4] = 0u;
+          }
+          // P^T over the first NC/2 of the NC S^T columns this thread read.
+          if constexpr (NC == 32) {
+            SPARGE_TMEM_ST_X16(sa, pk);
+          } else {
+            SPARGE_TMEM_ST_X8(sa, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(C::B_PPF + h));
+          // dS^T = P^T * (dP^T - D).
+          if (!warp_wait(bar(C::B_DPF + h), t & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (live) {
+            uint32_t dr[NC / 16][16];
+#pragma unroll
+            for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 64 + 16 * c, dr[c]);
+#pragma unroll
+            for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(dr[c]);
+            const float4* d4 = reinterpret_cast<const float4*>(rowv + 64 + NC * cg);
+#pragma unroll
+            for (int g = 0; g < NC / 4; ++g) {
+              const float4 dv4 = d4[g];
+              const float dq4[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+              float ds[4];
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const int col = g * 4 + q4;
+                ds[q4] = p[col] * (__uint_as_float(dr[col / 16][col % 16]) - dq4[q4]);
+              }
+              pk[g * 2 + 0] = pack_bf16x2(ds[0], ds[1]);
+              pk[g * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+            }
+          }
+          if constexpr (NC == 32) {
+            SPARGE_TMEM_ST_X16(sa + 64, pk);
+          } else {
+            SPARGE_TMEM_ST_X8(sa + 64, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(C::B_DSF + h));
+        }
+      }
+      if (!ok) break;
+      // Epilogue: lane r holds key r of dV and dK; warp group cg writes its
+      // share of the features, then releases the accumulators to the next
+      // tile's first MMAs.
+      if (!warp_wait(bar(C::B_RKF + 1), (t - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll 1
-    constexpr int FPW = D / (Roles<kDkdvWarps>::kCompute / 4);  // features per warp
-    for (int cc = cg * FPW; cc < (cg + 1) * FPW; cc += 16) {
-      uint32_t rv_[16], rk_[16];
-      if (have) {
+      for (int cc = cg * FPW; cc < (cg + 1) * FPW; cc += 16) {
+        uint32_t rv_[16], rk_[16];
         SPARGE_TMEM_LD_X16(lane_base + C::col_dv + cc, rv_);
         SPARGE_TMEM_LD_X16(lane_base + C::col_dk + cc, rk_);
         SPARGE_TMEM_WAIT_LD16(rv_);
         SPARGE_TMEM_WAIT_LD16(rk_);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) rv_[c] = rk_[c] = 0u;
-      }
-      if (key_in) {
-        uint4 v0, v1, k0, k1;
-        v0.x = pack_bf16x2(__uint_as_float(rv_[0]), __uint_as_float(rv_[1]));
-        v0.y = pack_bf16x2(__uint_as_float(rv_[2]), __uint_as_float(rv_[3]));
-        v0.z = pack_bf16x2(__uint_as_float(rv_[4]), __uint_as_float(rv_[5]));
-        v0.w = pack_bf16x2(__uint_as_float(rv_[6]), __uint_as_float(rv_[7]));
-        v1.x = pack_bf16x2(__uint_as_float(rv_[8]), __uint_as_float(rv_[9]));
-        v1.y = pack_bf16x2(__uint_as_float(rv_[10]), __uint_as_float(rv_[11]));
-        v1.z = pack_bf16x2(__uint_as_float(rv_[12]), __uint_as_float(rv_[13]));
-        v1.w = pack_bf16x2(__uint_as_float(rv_[14]), __uint_as_float(rv_[15]));
-        k0.x = pack_bf16x2(__uint_as_float(rk_[0]) * scale, __uint_as_float(rk_[1]) * scale);
-        k0.y = pack_bf16x2(__uint_as_float(rk_[2]) * scale, __uint_as_float(rk_[3]) * scale);
-        k0.z = pack_bf16x2(__uint_as_float(rk_[4]) * scale, __uint_as_float(rk_[5]) * scale);
-        k0.w = pack_bf16x2(__uint_as_float(rk_[6]) * scale, __uint_as_float(rk_[7]) * scale);
-        k1.x = pack_bf16x2(__uint_as_float(rk_[8]) * scale, __uint_as_float(rk_[9]) * scale);
-        k1.y = pack_bf16x2(__uint_as_float(rk_[10]) * scale, __uint_as_float(rk_[11]) * scale);
-        k1.z = pack_bf16x2(__uint_as_float(rk_[12]) * scale, __uint_as_float(rk_[13]) * scale);
-        k1.w = pack_bf16x2(__uint_as_float(rk_[14]) * scale, __uint_as_float(rk_[15]) * scale);
-        __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc), v0);
-        __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc + 8), v1);
-        __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc), k0);
-        __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc + 8), k1);
+        if (cc + 16 >= (cg + 1) * FPW) {
+          tc_fence_before();
+          mbar_arrive(bar(C::B_DKE));
+        }
+        if (key_in) {
+          uint4 v0, v1, k0, k1;
+          v0.x = pack_bf16x2(__uint_as_float(rv_[0]), __uint_as_float(rv_[1]));
+          v0.y = pack_bf16x2(__uint_as_float(rv_[2]), __uint_as_float(rv_[3]));
+          v0.z = pack_bf16x2(__uint_as_float(rv_[4]), __uint_as_float(rv_[5]));
+          v0.w = pack_bf16x2(__uint_as_float(rv_[6]), __uint_as_float(rv_[7]));
+          v1.x = pack_bf16x2(__uint_as_float(rv_[8]), __uint_as_float(rv_[9]));
+          v1.y = pack_bf16x2(__uint_as_float(rv_[10]), __uint_as_float(rv_[11]));
+          v1.z = pack_bf16x2(__uint_as_float(rv_[12]), __uint_as_float(rv_[13]));
+          v1.w = pack_bf16x2(__uint_as_float(rv_[14]), __uint_as_float(rv_[15]));
+          k0.x = pack_bf16x2(__uint_as_float(rk_[0]) * scale, __uint_as_float(rk_[1]) * scale);
+          k0.y = pack_bf16x2(__uint_as_float(rk_[2]) * scale, __uint_as_float(rk_[3]) * scale);
+          k0.z = pack_bf16x2(__uint_as_float(rk_[4]) * scale, __uint_as_float(rk_[5]) * scale);
+          k0.w = pack_bf16x2(__uint_as_float(rk_[6]) * scale, __uint_as_float(rk_[7]) * scale);
+          k1.x = pack_bf16x2(__uint_as_float(rk_[8]) * scale, __uint_as_float(rk_[9]) * scale);
+          k1.y = pack_bf16x2(__uint_as_float(rk_[10]) * scale, __uint_as_float(rk_[11]) * scale);
+          k1.z = pack_bf16x2(__uint_as_float(rk_[12]) * scale, __uint_as_float(rk_[13]) * scale);
+          k1.w = pack_bf16x2(__uint_as_float(rk_[14]) * scale, __uint_as_float(rk_[15]) * scale);
+          __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc), v0);
+          __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc + 8), v1);
+          __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc), k0);
+          __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc + 8), k1);
+        }
       }
     }
+    if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == Roles<kDkdvWarps>::kIssueA) {
+  if (warp == R::kIssueA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::tmem_cols);
   }
@@ -1106,13 +1223,21 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
     return cudaErrorInvalidValue;
   const float scale_log2 = scale * kLog2e;
 
+  // Both gradient kernels are persistent: one CTA per SM (or per work item
+  // when there are fewer), taking items from their work counters.
+  int dev = 0, nsm = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DkdvCfg<D>::smem_alloc);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<D><<<static_cast<unsigned>((long long)g.BH * Mt), Roles<kDkdvWarps>::kThreads,
-                       DkdvCfg<D>::smem_alloc, st>>>(
-      tq64, tk, tv, tdo64, lse, delta, col_idx, col_cnt, ws.col_order, g.N, g.Mq, g.Mk, Mt,
-      kv_per_tile, scale, scale_log2, static_cast<__nv_bfloat16*>(dk),
+  const int ntiles = g.BH * Mt;
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>(max(1, min(ntiles, nsm))),
+                       Roles<kDkdvWarps>::kThreads, DkdvCfg<D>::smem_alloc, st>>>(
+      tq64, tk, tv, tdo64, lse, delta, col_idx, col_cnt, ws.col_order, ntiles, ws.work + 1, g.N,
+      g.Mq, g.Mk, Mt, kv_per_tile, scale, scale_log2, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -1122,12 +1247,6 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: the dQ CTAs may start while the last dK/dV
   // CTAs run (D and the launch orders were complete before dK/dV started).
-  // Persistent: one CTA per SM (or per q-block when there are fewer).
-  int dev = 0, nsm = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
   const int nq = g.BH * g.Mq;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(max(1, min(nq, nsm))));
