@@ -47,9 +47,9 @@ METRIC = ("sparse attn fwd+bwd ms & kept-FLOP TFLOP/s at 95% sparsity; "
 KERNELS_PER_STEP = 8  # pool, logits, select, csc, fwd, delta (+ launch orders), dkdv, dq
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes per call of each entry point (dram__bytes_read.sum + dram__bytes_write.sum
-# summed over its kernels) from one ncu capture of the default workload (480p, k = 5 %,
-# p = 0) with the current kernels; reported as roofline.traffic on that workload only.
-NCU_TRAFFIC_BYTES = {("wan480", 0.05, 0.0): {"bwd": 1525.1e6, "fwd": 344.2e6, "mask": 214.5e6}}
+# summed over its kernels) from one ncu capture of the default workload (480p, 128 x 64
+# blocks, k = 5 %, p = 0) with the current kernels; reported as roofline.traffic on that workload only.
+NCU_TRAFFIC_BYTES = {("wan480", 64, 0.05, 0.0): {"bwd": 1591.5e6, "fwd": 343.8e6, "mask": 217.1e6}}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -438,7 +438,7 @@ def run_ours(args, wl, k_frac, p):
                                        "frac": r["achieved"] / tc_other}
     dom = max(part_ms, key=part_ms.get)
     roofline = dict(roof[dom])
-    roofline["traffic"] = NCU_TRAFFIC_BYTES.get((wl.name, k_frac, p), {}).get(dom)
+    roofline["traffic"] = NCU_TRAFFIC_BYTES.get((wl.name, wl.block_kv, k_frac, p), {}).get(dom)
     roofline["traffic_unit"] = "bytes per call (ncu)"
     roofline["per_launch_ms"] = part_ms[dom]
     roofline["algorithmic"] = {"fwd": "4*d per kept valid (query, key) pair",

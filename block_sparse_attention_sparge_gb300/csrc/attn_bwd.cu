@@ -159,18 +159,6 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(
   if (c == 0 && r < rows) delta[r] = s;
 }
 
-// tcgen05.mma kind::f16 with the A operand in tensor memory (M lanes, K/2
-// 32-bit columns holding bf16 pairs, element 2c in the low half of column c).
-__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Loads 32 consecutive fp32 TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32u(uint32_t addr, uint32_t (&a)[16], uint32_t (&b)[16]) {
   SPARGE_TMEM_LD_X16(addr, a);
@@ -305,7 +293,7 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
   // producer through the ring (tile -1: no more work, -2: the producer gave up).
   auto next_tile = [&](int seq, bool ok, int* n) -> int {
     const int rs = seq % C::NRING;
-    if (!ok || !mbar_wait(bar(C::B_IF + rs), (seq / C::NRING) & 1, kWaitTimeoutNs)) return -2;
+    if (!ok || !warp_wait(bar(C::B_IF + rs), (seq / C::NRING) & 1)) return -2;
     *n = ring[2 * rs + 1];
     return ring[2 * rs];
   };
@@ -451,128 +439,125 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
   } else if (warp == R::kIssueA) {
     // ---------------------------------------------------------- S^T, dP^T
     // S^T_h = K Q_h^T and dP^T_h = V dO_h^T (M = 128 keys, N = 64 queries of
-    // half h, K = d).
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(kPair, 64, false, false);
-      const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(s0 + C::off_v, 16, 1024);
-      bool ok = true;
-      int t = 0, j = 0;
-      for (int seq = 0;; ++seq) {
-        int n = 0;
-        const int it = next_tile(seq, ok, &n);
-        release_tile(seq);
-        if (it < 0) {
-          if (it == -2) ok = false;
-          break;
-        }
-        if (n == 0) continue;
-        if (!mbar_wait(bar(C::B_KV), j & 1, kWaitTimeoutNs)) {
-          ok = false;
-          break;
-        }
-        ++j;
-        for (int e = 0; ok && e < n; ++e, ++t) {
-          for (int h = 0; h < 2; ++h) {
-            const int k = 2 * t + h, sl = k % C::NSLOT;
-            // S^T_h's columns hold P^T_h of entry t - 1 until its dV MMAs are
-            // done, dP^T_h's hold dS^T_h until its dK MMAs are.
-            if (!mbar_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1, kWaitTimeoutNs) ||
-                (t >= 1 && !mbar_wait(bar(C::B_RVF + h), (t - 1) & 1, kWaitTimeoutNs))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, 16, 1024);
-            const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, 16, 1024);
-            const uint32_t dS = tmem + h * 128;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
-              const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
-              tc_mma_bf16(dS, sdesc_add(dk0, ka), sdesc_add(dq, kb), idS, kk > 0);
-            }
-            tc_commit(bar(C::B_SSF + h));
-            if (t >= 1 && !mbar_wait(bar(C::B_RKF + h), (t - 1) & 1, kWaitTimeoutNs)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
-              const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
-              tc_mma_bf16(dS + 64, sdesc_add(dv0, ka), sdesc_add(ddo, kb), idS, kk > 0);
-            }
-            tc_commit(bar(C::B_DPF + h));
-          }
-        }
-        if (!ok) break;
-        tc_commit(bar(C::B_KVE));  // every S^T and dP^T of this tile issued
+    // half h, K = d).  The whole warp runs the loop; one elected lane issues
+    // each MMA.
+    constexpr uint32_t idS = idesc_bf16(kPair, 64, false, false);
+    const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
+    const uint64_t dv0 = sdesc_sw128(s0 + C::off_v, 16, 1024);
+    bool ok = true;
+    int t = 0, j = 0;
+    for (int seq = 0;; ++seq) {
+      int n = 0;
+      const int it = next_tile(seq, ok, &n);
+      if (lane == 0) release_tile(seq);
+      if (it < 0) {
+        if (it == -2) ok = false;
+        break;
       }
-      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      tc_commit(bar(C::B_DONE));
-      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+      if (n == 0) continue;
+      if (!warp_wait(bar(C::B_KV), j & 1)) {
+        ok = false;
+        break;
+      }
+      ++j;
+      for (int e = 0; ok && e < n; ++e, ++t) {
+        for (int h = 0; h < 2; ++h) {
+          const int k = 2 * t + h, sl = k % C::NSLOT;
+          // S^T_h's columns hold P^T_h of entry t - 1 until its dV MMAs are
+          // done, dP^T_h's hold dS^T_h until its dK MMAs are.
+          if (!warp_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1) ||
+              (t >= 1 && !warp_wait(bar(C::B_RVF + h), (t - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, 16, 1024);
+          const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, 16, 1024);
+          const uint32_t dS = tmem + h * 128;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+            const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
+            warp_mma_bf16(dS, sdesc_add(dk0, ka), sdesc_add(dq, kb), idS, kk > 0);
+          }
+          warp_commit(bar(C::B_SSF + h));
+          if (t >= 1 && !warp_wait(bar(C::B_RKF + h), (t - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+            const uint32_t kb = (kk >> 2) * C::kChunkH + (kk & 3) * 32;
+            warp_mma_bf16(dS + 64, sdesc_add(dv0, ka), sdesc_add(ddo, kb), idS, kk > 0);
+          }
+          warp_commit(bar(C::B_DPF + h));
+        }
+      }
+      if (!ok) break;
+      warp_commit(bar(C::B_KVE));  // every S^T and dP^T of this tile issued
     }
+    if (!ok && lane == 0) report_error(status, SPARGE_ERR_TIMEOUT);
+    warp_commit(bar(C::B_DONE));
+    warp_wait(bar(C::B_DONE), 0);
   } else if (warp == R::kIssueB) {
     // ---------------------------------------------------------- dV, dK
     // dV += P^T_h dO_h and dK += dS^T_h Q_h (M = 128 keys, N = d, K = the 64
     // queries of half h); A from TMEM, B = dO_h / Q_h read MN-major.  The
     // first MMAs of a tile overwrite the accumulators, after the compute
     // warps have read out the previous tile's.
-    if (lane == 0) {
-      constexpr uint32_t idG = idesc_bf16(kPair, D, false, true);
-      constexpr int NC = 64 / (R::kCompute / 4);
-      bool ok = true;
-      int t = 0, j = 0;
-      for (int seq = 0;; ++seq) {
-        int n = 0;
-        const int it = next_tile(seq, ok, &n);
-        release_tile(seq);
-        if (it < 0) {
-          if (it == -2) ok = false;
-          break;
-        }
-        if (n == 0) continue;
-        for (int e = 0; ok && e < n; ++e, ++t) {
-          for (int h = 0; h < 2; ++h) {
-            const int sl = (2 * t + h) % C::NSLOT;
-            const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, C::kChunkH, 1024);
-            const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, C::kChunkH, 1024);
-            const uint32_t ap = tmem + h * 128;
-            const bool first = e == 0 && h == 0;
-            if (!mbar_wait(bar(C::B_PPF + h), t & 1, kWaitTimeoutNs) ||
-                (first && j >= 1 && !mbar_wait(bar(C::B_DKE), (j - 1) & 1, kWaitTimeoutNs))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // Queries 16kk .. 16kk + 15 of the half: the TMEM columns where the
-            // compute warp group holding them wrote their bf16 pairs.
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_bf16_ta(tmem + C::col_dv, ap + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
-                             sdesc_add(ddo, kk * 2048), idG, (!first || kk > 0) ? 1u : 0u);
-            tc_commit(bar(C::B_RVF + h));
-            if (!mbar_wait(bar(C::B_DSF + h), t & 1, kWaitTimeoutNs)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_bf16_ta(tmem + C::col_dk, ap + 64 + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
-                             sdesc_add(dq, kk * 2048), idG, (!first || kk > 0) ? 1u : 0u);
-            tc_commit(bar(C::B_RKF + h));
-            tc_commit(bar(C::B_QE + sl));
-          }
-        }
-        ++j;
+    constexpr uint32_t idG = idesc_bf16(kPair, D, false, true);
+    constexpr int NC = 64 / (R::kCompute / 4);
+    bool ok = true;
+    int t = 0, j = 0;
+    for (int seq = 0;; ++seq) {
+      int n = 0;
+      const int it = next_tile(seq, ok, &n);
+      if (lane == 0) release_tile(seq);
+      if (it < 0) {
+        if (it == -2) ok = false;
+        break;
       }
-      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      tc_commit(bar(C::B_DONE));
-      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+      if (n == 0) continue;
+      for (int e = 0; ok && e < n; ++e, ++t) {
+        for (int h = 0; h < 2; ++h) {
+          const int sl = (2 * t + h) % C::NSLOT;
+          const uint64_t dq = sdesc_sw128(s0 + C::off_q + sl * C::kQh, C::kChunkH, 1024);
+          const uint64_t ddo = sdesc_sw128(s0 + C::off_do + sl * C::kQh, C::kChunkH, 1024);
+          const uint32_t ap = tmem + h * 128;
+          const bool first = e == 0 && h == 0;
+          if (!warp_wait(bar(C::B_PPF + h), t & 1) ||
+              (first && j >= 1 && !warp_wait(bar(C::B_DKE), (j - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // Queries 16kk .. 16kk + 15 of the half: the TMEM columns where the
+          // compute warp group holding them wrote their bf16 pairs.
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            warp_mma_bf16_ta(tmem + C::col_dv, ap + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
+                             sdesc_add(ddo, kk * 2048), idG, (!first || kk > 0) ? 1u : 0u);
+          warp_commit(bar(C::B_RVF + h));
+          if (!warp_wait(bar(C::B_DSF + h), t & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            warp_mma_bf16_ta(tmem + C::col_dk, ap + 64 + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
+                             sdesc_add(dq, kk * 2048), idG, (!first || kk > 0) ? 1u : 0u);
+          warp_commit(bar(C::B_RKF + h));
+          warp_commit(bar(C::B_QE + sl));
+        }
+      }
+      ++j;
     }
+    if (!ok && lane == 0) report_error(status, SPARGE_ERR_TIMEOUT);
+    warp_commit(bar(C::B_DONE));
+    warp_wait(bar(C::B_DONE), 0);
   } else if (warp < R::kCompute) {
     // ---------------------------------------------------------- compute
     // Thread = key row r (TMEM lane).  All compute warps take half 0 of an
@@ -857,10 +842,11 @@ __global__ void __launch_bounds__(Roles<kDqWarps>::kThreads, 1)
 
   // The q-block handed out as the seq-th of this CTA (-1: no more work).  The
   // producer fetches ids from the counter into a ring; the other roles read
-  // them from there, in the same order.
+  // them from there, in the same order (whole warps: the result is
+  // warp-uniform).
   auto next_item = [&](int seq, bool ok) -> int {
     const int rs = seq % C::NRING;
-    if (!ok || !mbar_wait(bar(C::B_IF + rs), (seq / C::NRING) & 1, kWaitTimeoutNs)) return -2;
+    if (!ok || !warp_wait(bar(C::B_IF + rs), (seq / C::NRING) & 1)) return -2;
     const int it = ring[rs];
     return it;
   };
@@ -926,16 +912,7 @@ __global__ void __launch_bounds__(Roles<kDqWarps>::kThreads, 1)
             rw[half] = half_row(x, u, half);
             if (rw[half] < 0) rw[half] = Mk * kBN;  // empty half: rows past N read as zeros
           }
-          if (g >= C::NSV &&
-              !mbar_wait(bar(C::B_VE + sv), ((g / C::NSV) - 1) & 1, kWaitTimeoutNs)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(C::B_VF + sv), C::kKP);
-          for (int half = 0; half < 2; ++half)
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d(s0 + C::off_v + sv * C::kKP + c * C::kChunkK + half * kBN * 128, &tmV,
-                          bar(C::B_VF + sv), c * 64, rw[half], x.bh);
+          // K first: S of this step needs it before dP needs V.
           if (g >= C::NSK &&
               !mbar_wait(bar(C::B_KE + sk), ((g / C::NSK) - 1) & 1, kWaitTimeoutNs)) {
             ok = false;
@@ -946,6 +923,16 @@ __global__ void __launch_bounds__(Roles<kDqWarps>::kThreads, 1)
             for (int c = 0; c < D / 64; ++c)
               tma_load_3d(s0 + C::off_k + sk * C::kKP + c * C::kChunkK + half * kBN * 128, &tmK,
                           bar(C::B_KF + sk), c * 64, rw[half], x.bh);
+          if (g >= C::NSV &&
+              !mbar_wait(bar(C::B_VE + sv), ((g / C::NSV) - 1) & 1, kWaitTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::B_VF + sv), C::kKP);
+          for (int half = 0; half < 2; ++half)
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(s0 + C::off_v + sv * C::kKP + c * C::kChunkK + half * kBN * 128, &tmV,
+                          bar(C::B_VF + sv), c * 64, rw[half], x.bh);
         }
       }
       if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
@@ -960,109 +947,106 @@ __global__ void __launch_bounds__(Roles<kDqWarps>::kThreads, 1)
     // ---------------------------------------------------------- S, dP
     // S_g = Q K_g^T into TMEM buffer g % 2 (free once dQ of step g - 2 has
     // read its dS), then dP_g = dO V_g^T (its region frees once the compute
-    // warps have read dP of step g - 1).  M = 128 queries, N = 128 keys.
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(kBM, kPair, false, false);
-      const uint64_t dq0 = sdesc_sw128(s0 + C::off_q, 16, 1024);
-      const uint64_t ddo0 = sdesc_sw128(s0 + C::off_do, 16, 1024);
-      bool ok = true;
-      int g = 0, j = 0;
-      for (int seq = 0;; ++seq) {
-        const int it = next_item(seq, ok);
-        release_item(seq);
-        if (it < 0) {
-          if (it == -2) ok = false;
-          break;
-        }
-        const Item x = item_info(it);
-        if (x.n == 0) continue;
-        if (!mbar_wait(bar(C::B_Q), j & 1, kWaitTimeoutNs)) {
+    // warps have read dP of step g - 1).  M = 128 queries, N = 128 keys.  The
+    // whole warp runs the loop; one elected lane issues each MMA.
+    constexpr uint32_t idS = idesc_bf16(kBM, kPair, false, false);
+    const uint64_t dq0 = sdesc_sw128(s0 + C::off_q, 16, 1024);
+    const uint64_t ddo0 = sdesc_sw128(s0 + C::off_do, 16, 1024);
+    bool ok = true;
+    int g = 0, j = 0;
+    for (int seq = 0;; ++seq) {
+      const int it = next_item(seq, ok);
+      if (lane == 0) release_item(seq);
+      if (it < 0) {
+        if (it == -2) ok = false;
+        break;
+      }
+      const Item x = item_info(it);
+      if (x.n == 0) continue;
+      if (!warp_wait(bar(C::B_Q), j & 1)) {
+        ok = false;
+        break;
+      }
+      ++j;
+      for (int u = 0; ok && u < x.npair; ++u, ++g) {
+        const int sk = g % C::NSK, sv = g % C::NSV, b = g & 1;
+        if (!warp_wait(bar(C::B_KF + sk), (g / C::NSK) & 1) ||
+            (g >= 2 && !warp_wait(bar(C::B_SE + b), ((g >> 1) - 1) & 1))) {
           ok = false;
           break;
         }
-        ++j;
-        for (int u = 0; ok && u < x.npair; ++u, ++g) {
-          const int sk = g % C::NSK, sv = g % C::NSV, b = g & 1;
-          if (!mbar_wait(bar(C::B_KF + sk), (g / C::NSK) & 1, kWaitTimeoutNs) ||
-              (g >= 2 && !mbar_wait(bar(C::B_SE + b), ((g >> 1) - 1) & 1, kWaitTimeoutNs))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, 16, 1024);
+        tc_fence_after();
+        const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
-            const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
-            tc_mma_bf16(tmem + C::col_s + 128 * b, sdesc_add(dq0, ka), sdesc_add(dkd, kb), idS,
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
+          const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+          warp_mma_bf16(tmem + C::col_s + 128 * b, sdesc_add(dq0, ka), sdesc_add(dkd, kb), idS,
                         kk > 0);
-          }
-          tc_commit(bar(C::B_SF + b));
-          if (!mbar_wait(bar(C::B_VF + sv), (g / C::NSV) & 1, kWaitTimeoutNs) ||
-              (g >= 1 && !mbar_wait(bar(C::B_DPE), (g - 1) & 1, kWaitTimeoutNs))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t dvd = sdesc_sw128(s0 + C::off_v + sv * C::kKP, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
-            const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
-            tc_mma_bf16(tmem + C::col_dp, sdesc_add(ddo0, ka), sdesc_add(dvd, kb), idS, kk > 0);
-          }
-          tc_commit(bar(C::B_DPF));
-          tc_commit(bar(C::B_VE + sv));
         }
-        if (!ok) break;
-        tc_commit(bar(C::B_QE));  // every S and dP of this q-block issued
+        warp_commit(bar(C::B_SF + b));
+        if (!warp_wait(bar(C::B_VF + sv), (g / C::NSV) & 1) ||
+            (g >= 1 && !warp_wait(bar(C::B_DPE), (g - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t dvd = sdesc_sw128(s0 + C::off_v + sv * C::kKP, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * C::kChunkQ + (kk & 3) * 32;
+          const uint32_t kb = (kk >> 2) * C::kChunkK + (kk & 3) * 32;
+          warp_mma_bf16(tmem + C::col_dp, sdesc_add(ddo0, ka), sdesc_add(dvd, kb), idS, kk > 0);
+        }
+        warp_commit(bar(C::B_DPF));
+        warp_commit(bar(C::B_VE + sv));
       }
-      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      tc_commit(bar(C::B_DONE));
-      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+      if (!ok) break;
+      warp_commit(bar(C::B_QE));  // every S and dP of this q-block issued
     }
+    if (!ok && lane == 0) report_error(status, SPARGE_ERR_TIMEOUT);
+    warp_commit(bar(C::B_DONE));
+    warp_wait(bar(C::B_DONE), 0);
   } else if (warp == R::kIssueB) {
     // ---------------------------------------------------------- dQ
     // dQ += dS_g K_g (A = dS from TMEM buffer g % 2, K = 128 keys; B = the key
     // tile read MN-major, N = d).  dS of keys 16kk .. 16kk + 15 sits in the
     // buffer's columns 32 (kk / 2) + 8 (kk % 2) .. + 7.  The first step of a
     // q-block waits until the previous one's accumulator has been read out.
-    if (lane == 0) {
-      constexpr uint32_t idQ = idesc_bf16(kBM, D, false, true);
-      bool ok = true;
-      int g = 0, j = 0;
-      for (int seq = 0;; ++seq) {
-        const int it = next_item(seq, ok);
-        release_item(seq);
-        if (it < 0) {
-          if (it == -2) ok = false;
+    constexpr uint32_t idQ = idesc_bf16(kBM, D, false, true);
+    bool ok = true;
+    int g = 0, j = 0;
+    for (int seq = 0;; ++seq) {
+      const int it = next_item(seq, ok);
+      if (lane == 0) release_item(seq);
+      if (it < 0) {
+        if (it == -2) ok = false;
+        break;
+      }
+      const Item x = item_info(it);
+      if (x.n == 0) continue;
+      for (int u = 0; ok && u < x.npair; ++u, ++g) {
+        const int sk = g % C::NSK, b = g & 1;
+        if (!warp_wait(bar(C::B_DSF + b), (g >> 1) & 1) ||
+            (u == 0 && j >= 1 && !warp_wait(bar(C::B_DQE), (j - 1) & 1))) {
+          ok = false;
           break;
         }
-        const Item x = item_info(it);
-        if (x.n == 0) continue;
-        for (int u = 0; ok && u < x.npair; ++u, ++g) {
-          const int sk = g % C::NSK, b = g & 1;
-          if (!mbar_wait(bar(C::B_DSF + b), (g >> 1) & 1, kWaitTimeoutNs) ||
-              (u == 0 && j >= 1 && !mbar_wait(bar(C::B_DQE), (j - 1) & 1, kWaitTimeoutNs))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, C::kChunkK, 1024);
-          const uint32_t ads = tmem + C::col_s + 128 * b;
+        tc_fence_after();
+        const uint64_t dkd = sdesc_sw128(s0 + C::off_k + sk * C::kKP, C::kChunkK, 1024);
+        const uint32_t ads = tmem + C::col_s + 128 * b;
 #pragma unroll
-          for (int kk = 0; kk < kPair / 16; ++kk)
-            tc_mma_bf16_ta(tmem + C::col_dq, ads + (kk >> 1) * 32 + (kk & 1) * 8,
+        for (int kk = 0; kk < kPair / 16; ++kk)
+          warp_mma_bf16_ta(tmem + C::col_dq, ads + (kk >> 1) * 32 + (kk & 1) * 8,
                            sdesc_add(dkd, kk * 2048), idQ, (u > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(C::B_SE + b));
-          tc_commit(bar(C::B_KE + sk));
-        }
-        ++j;
+        warp_commit(bar(C::B_SE + b));
+        warp_commit(bar(C::B_KE + sk));
       }
-      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      tc_commit(bar(C::B_DONE));
-      mbar_wait(bar(C::B_DONE), 0, kWaitTimeoutNs);
+      ++j;
     }
+    if (!ok && lane == 0) report_error(status, SPARGE_ERR_TIMEOUT);
+    warp_commit(bar(C::B_DONE));
+    warp_wait(bar(C::B_DONE), 0);
   } else if (warp < R::kCompute) {
     // ---------------------------------------------------------- compute
     // Thread = query row r (TMEM lane); warp group c = warp / 4 takes keys

@@ -86,17 +86,6 @@ struct FwdCfg {
   static constexpr uint32_t col_o = 128;
 };
 
-// tcgen05.mma kind::f16 with the A operand in tensor memory (M lanes, K/2
-// 32-bit columns holding bf16 pairs, element 2c in the low half of column c).
-__device__ __forceinline__ void tc_mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                                   uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
@@ -123,10 +112,12 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
   const int32_t* list = row_idx + row_id * Mk;
   // Steps of 64 keys: one per kept block of 64 keys, two per kept block of
   // 128 (its halves).  First key row of step t:
-  const int sub = bk / kBN;
-  const int n = nkv * sub;
+  // bk is 64 or 128 (checked by the host), so a step index splits by a shift.
+  const int sub_shift = bk > kBN ? 1 : 0;
+  const int n = nkv << sub_shift;
   auto row_of = [&](int t) -> int {
-    return min(max(__ldg(list + t / sub), 0), Mk - 1) * bk + (t % sub) * kBN;
+    return min(max(__ldg(list + (t >> sub_shift)), 0), Mk - 1) * bk +
+           (t & sub_shift) * kBN;
   };
 
   if (threadIdx.x == 0) {
@@ -187,16 +178,17 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
     }
   } else if (warp == kSWarp) {
     // ------------------------------------------------------------ S issuer
-    if (lane == 0 && n > 0) {
+    // The whole warp runs the loop; one elected lane issues each MMA.
+    if (n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, kBN, false, false);
       const uint64_t dq0 = sdesc_sw128(s0 + C::off_q, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
-      bool ok = mbar_wait(bar(C::B_Q), 0, kWaitTimeoutNs);
+      bool ok = warp_wait(bar(C::B_Q), 0);
       for (int t = 0; ok && t < n; ++t) {
         const int s = t % C::NST;
         // TMEM tile t & 1 holds P(t - 2) until PV(t - 2) has completed.
-        if (!mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs) ||
-            (t >= 2 && !mbar_wait(bar(C::B_PV + (t & 1)), ((t - 2) >> 1) & 1, kWaitTimeoutNs))) {
+        if (!warp_wait(bar(C::B_KF + s), (t / C::NST) & 1) ||
+            (t >= 2 && !warp_wait(bar(C::B_PV + (t & 1)), ((t - 2) >> 1) & 1))) {
           ok = false;
           break;
         }
@@ -206,26 +198,26 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
-          tc_mma_bf16(dS, sdesc_add(dq0, (kk >> 2) * (kBM * 128) + koff),
-                      sdesc_add(dk, (kk >> 2) * (kBN * 128) + koff), idS, kk > 0);
+          warp_mma_bf16(dS, sdesc_add(dq0, (kk >> 2) * (kBM * 128) + koff),
+                        sdesc_add(dk, (kk >> 2) * (kBN * 128) + koff), idS, kk > 0);
         }
-        tc_commit(bar(C::B_SF + (t & 1)));
-        tc_commit(bar(C::B_KE + s));
+        warp_commit(bar(C::B_SF + (t & 1)));
+        warp_commit(bar(C::B_KE + s));
       }
-      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      // Drain: every MMA this thread issued has completed once this arrives.
-      tc_commit(bar(C::B_DRAIN));
-      mbar_wait(bar(C::B_DRAIN), 0, kWaitTimeoutNs);
+      if (!ok && lane == 0) report_error(status, SPARGE_ERR_TIMEOUT);
+      // Drain: every MMA this warp issued has completed once this arrives.
+      warp_commit(bar(C::B_DRAIN));
+      warp_wait(bar(C::B_DRAIN), 0);
     }
   } else if (warp == kPVWarp) {
     // ------------------------------------------------------------ PV issuer
-    if (lane == 0 && n > 0) {
+    if (n > 0) {
       constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
       bool ok = true;
       for (int u = 0; ok && u < n; ++u) {
         const int su = u % C::NST;
-        if (!mbar_wait(bar(C::B_PF + (u % C::NP)), (u / C::NP) & 1, kWaitTimeoutNs) ||
-            !mbar_wait(bar(C::B_VF + su), (u / C::NST) & 1, kWaitTimeoutNs)) {
+        if (!warp_wait(bar(C::B_PF + (u % C::NP)), (u / C::NP) & 1) ||
+            !warp_wait(bar(C::B_VF + su), (u / C::NST) & 1)) {
           ok = false;
           break;
         }
@@ -234,14 +226,14 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
         const uint64_t dv = sdesc_sw128(s0 + C::off_v + su * C::kKV, kBN * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          tc_mma_bf16_tmem_a(tmem + C::col_o, ap + kk * 8, sdesc_add(dv, kk * 16 * 128), idO,
-                             (u > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(C::B_VE + su));
-        tc_commit(bar(C::B_PV + (u & 1)));
+          warp_mma_bf16_ta(tmem + C::col_o, ap + kk * 8, sdesc_add(dv, kk * 16 * 128), idO,
+                           (u > 0 || kk > 0) ? 1u : 0u);
+        warp_commit(bar(C::B_VE + su));
+        warp_commit(bar(C::B_PV + (u & 1)));
       }
-      if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
-      tc_commit(bar(C::B_DRAIN));
-      mbar_wait(bar(C::B_DRAIN), 0, kWaitTimeoutNs);
+      if (!ok && lane == 0) report_error(status, SPARGE_ERR_TIMEOUT);
+      warp_commit(bar(C::B_DRAIN));
+      warp_wait(bar(C::B_DRAIN), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
