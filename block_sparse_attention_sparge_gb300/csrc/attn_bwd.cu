@@ -189,7 +189,7 @@ template <int D>
 struct DkdvCfg {
   // Q and dO arrive per 64-query half of a q-block: a slot holds Q_h and dO_h
   // (64 rows each) and is released once the gradient MMAs of that half are done.
-  static constexpr int NSLOT = D == 128 ? 4 : 8;
+  static constexpr int NSLOT = D == 128 ? 5 : 8;
   static constexpr int NRING = 4;                    // key tiles handed out ahead
   static constexpr uint32_t kKP = kPair * D * 2;     // K (or V) of the 128 keys
   static constexpr uint32_t kQh = 64 * D * 2;        // one Q (or dO) half tile
@@ -199,7 +199,7 @@ struct DkdvCfg {
   static constexpr uint32_t off_v = off_k + kKP;
   static constexpr uint32_t off_q = off_v + kKP;               // NSLOT Q halves
   static constexpr uint32_t off_do = off_q + NSLOT * kQh;      // NSLOT dO halves
-  static constexpr uint32_t off_row = off_do + NSLOT * kQh;    // NSLOT x {lse*log2e [64], D [64]}
+  static constexpr uint32_t off_row = off_do + NSLOT * kQh;    // NSLOT x {-lse*log2e [64], -D [64]}
   static constexpr uint32_t off_info = off_row + NSLOT * 2 * 64 * 4;  // NSLOT x int32
   static constexpr uint32_t off_ring = off_info + 64;          // NRING x {tile, entries}
   static constexpr uint32_t off_bar = off_ring + 64;
@@ -222,7 +222,10 @@ struct DkdvCfg {
   static constexpr int NBAR = B_DONE + 1;
   static constexpr uint32_t off_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_slot + 16;
-  static constexpr uint32_t smem_alloc = bytes + 1024;
+  // The dynamic shared-memory window starts 1024-byte aligned on sm_103a
+  // (checked at kernel entry), so no alignment pad is allocated: five Q/dO
+  // slots at d = 128 then fit.
+  static constexpr uint32_t smem_alloc = bytes;
   // TMEM: half h of the queries uses columns [128h, 128h + 128): S^T_h at
   // +0 (64 fp32 columns) and dP^T_h at +64.  P^T_h is written over S^T_h as
   // bf16 pairs: the compute group holding queries NC*g .. NC*g + NC - 1 (NC
@@ -256,10 +259,13 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
   // The dQ kernel (independent of this one) may start on SMs this grid's
   // last CTAs leave idle.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   const uint32_t s0 = smem_u32(sm);
+  if ((s0 & 1023u) != 0u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) report_error(status, SPARGE_ERR_CUDA);
+    return;
+  }
   auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + C::off_slot);
   int32_t* info = reinterpret_cast<int32_t*>(sm + C::off_info);
@@ -413,14 +419,14 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
             }
             info[sl] = ic | (flags << 24);
           }
-          // lse * log2(e) and D of the half's 64 tokens (queries past N get
-          // +inf and 0, so that their P and dS are 0).
+          // -lse * log2(e) and -D of the half's 64 tokens (queries past N get
+          // -inf and 0, so that their P and dS are 0).
           float2 l2, d2;
           const int tok = row0 + lane * 2;
-          l2.x = tok < N ? __ldg(lse_h + tok) * kLog2e : INFINITY;
-          l2.y = tok + 1 < N ? __ldg(lse_h + tok + 1) * kLog2e : INFINITY;
-          d2.x = tok < N ? __ldg(del_h + tok) : 0.f;
-          d2.y = tok + 1 < N ? __ldg(del_h + tok + 1) : 0.f;
+          l2.x = tok < N ? -__ldg(lse_h + tok) * kLog2e : -INFINITY;
+          l2.y = tok + 1 < N ? -__ldg(lse_h + tok + 1) * kLog2e : -INFINITY;
+          d2.x = tok < N ? -__ldg(del_h + tok) : 0.f;
+          d2.y = tok + 1 < N ? -__ldg(del_h + tok + 1) : 0.f;
           float* rowv = reinterpret_cast<float*>(sm + C::off_row + sl * (2 * 64 * 4));
           reinterpret_cast<float2*>(rowv)[lane] = l2;
           reinterpret_cast<float2*>(rowv + 64)[lane] = d2;
@@ -616,16 +622,20 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
             for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 16 * c, sr[c]);
 #pragma unroll
             for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(sr[c]);
-            const float4* l4 = reinterpret_cast<const float4*>(rowv + NC * cg);
+            // Two queries per packed instruction: P^T = 2^(S^T * scale*log2e - lse*log2e).
+            const uint64_t sl2 = f32x2(scale_log2, scale_log2);
+            const ulonglong2* l4 = reinterpret_cast<const ulonglong2*>(rowv + NC * cg);
 #pragma unroll
             for (int g = 0; g < NC / 4; ++g) {
-              const float4 lv = l4[g];
-              const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
+              const ulonglong2 lv = l4[g];  // -lse*log2e of queries 4g .. 4g + 3
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const int col = g * 4 + q4;
-                p[col] = ex2_approx(fmaf(__uint_as_float(sr[col / 16][col % 16]), scale_log2,
-                                         -lq[q4]));
+              for (int q2 = 0; q2 < 2; ++q2) {
+                const int col = g * 4 + 2 * q2;
+                const uint64_t x = ffma2(f32x2(__uint_as_float(sr[col / 16][col % 16]),
+                                               __uint_as_float(sr[col / 16][col % 16 + 1])),
+                                         sl2, q2 == 0 ? lv.x : lv.y);
+                p[col] = ex2_approx(f32x2_lo(x));
+                p[col + 1] = ex2_approx(f32x2_hi(x));
               }
             }
             if (!key_in) {
@@ -661,19 +671,20 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
             for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 64 + 16 * c, dr[c]);
 #pragma unroll
             for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(dr[c]);
-            const float4* d4 = reinterpret_cast<const float4*>(rowv + 64 + NC * cg);
+            // dS^T = P^T * (dP^T - D), two queries per packed instruction.
+            const ulonglong2* d4 = reinterpret_cast<const ulonglong2*>(rowv + 64 + NC * cg);
 #pragma unroll
             for (int g = 0; g < NC / 4; ++g) {
-              const float4 dv4 = d4[g];
-              const float dq4[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-              float ds[4];
+              const ulonglong2 dv4 = d4[g];  // -D of queries 4g .. 4g + 3
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const int col = g * 4 + q4;
-                ds[q4] = p[col] * (__uint_as_float(dr[col / 16][col % 16]) - dq4[q4]);
+              for (int q2 = 0; q2 < 2; ++q2) {
+                const int col = g * 4 + 2 * q2;
+                const uint64_t dd = fadd2(f32x2(__uint_as_float(dr[col / 16][col % 16]),
+                                                __uint_as_float(dr[col / 16][col % 16 + 1])),
+                                          q2 == 0 ? dv4.x : dv4.y);
+                const uint64_t z = fmul2(f32x2(p[col], p[col + 1]), dd);
+                pk[g * 2 + q2] = pack_bf16x2(f32x2_lo(z), f32x2_hi(z));
               }
-              pk[g * 2 + 0] = pack_bf16x2(ds[0], ds[1]);
-              pk[g * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
             }
           }
           if constexpr (NC == 32) {
@@ -1101,15 +1112,22 @@ __global__ void __launch_bounds__(Roles<kDqWarps>::kThreads, 1)
         tmem_ld32u(sb, sr, sr2);
         uint32_t pk[16];
         if (rv && valid == 32) {
+          // Two columns per packed instruction: P = 2^(S * scale*log2e - lse*log2e),
+          // dS = P * (dP - D).
+          const uint64_t sl2 = f32x2(scale_log2, scale_log2);
+          const uint64_t nl2 = f32x2(-lse2, -lse2);
+          const uint64_t nd2 = f32x2(-drow, -drow);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e] : sr2[e - 16]),
-                                             scale_log2, -lse2));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(e < 16 ? sr[e + 1] : sr2[e - 15]),
-                                             scale_log2, -lse2));
-            const float d_a = __uint_as_float(e < 16 ? dr[e] : dr2[e - 16]);
-            const float d_b = __uint_as_float(e < 16 ? dr[e + 1] : dr2[e - 15]);
-            pk[e / 2] = pack_bf16x2(p0 * (d_a - drow), p1 * (d_b - drow));
+            const uint64_t x = ffma2(f32x2(__uint_as_float(e < 16 ? sr[e] : sr2[e - 16]),
+                                           __uint_as_float(e < 16 ? sr[e + 1] : sr2[e - 15])),
+                                     sl2, nl2);
+            const uint64_t pp = f32x2(ex2_approx(f32x2_lo(x)), ex2_approx(f32x2_hi(x)));
+            const uint64_t dd = fadd2(f32x2(__uint_as_float(e < 16 ? dr[e] : dr2[e - 16]),
+                                            __uint_as_float(e < 16 ? dr[e + 1] : dr2[e - 15])),
+                                      nd2);
+            const uint64_t z = fmul2(pp, dd);
+            pk[e / 2] = pack_bf16x2(f32x2_lo(z), f32x2_hi(z));
           }
         } else {
 #pragma unroll
