@@ -283,20 +283,27 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
         for (int c = 0; c < kBN; ++c)
           if (c >= valid) x[c] = masked;
       }
-      // Row max as a tree over 8 independent partial maxima.
+      // Row max as a tree over 8 independent partial maxima, two new
+      // columns per three-input max.
       float mp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mp[e] = x[e];
       if (pos) {
 #pragma unroll
-        for (int c = 8; c < kBN; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-        mp[0] = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                      fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        for (int c = 8; c < 56; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mp[e] = fmax3(mp[e], x[c + e], x[c + 8 + e]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mp[e] = fmaxf(mp[e], x[56 + e]);
+        mp[0] = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
       } else {
 #pragma unroll
-        for (int c = 8; c < kBN; ++c) mp[c & 7] = fminf(mp[c & 7], x[c]);
-        mp[0] = fminf(fminf(fminf(mp[0], mp[1]), fminf(mp[2], mp[3])),
-                      fminf(fminf(mp[4], mp[5]), fminf(mp[6], mp[7])));
+        for (int c = 8; c < 56; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mp[e] = fmin3(mp[e], x[c + e], x[c + 8 + e]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mp[e] = fminf(mp[e], x[56 + e]);
+        mp[0] = fmin3(fmin3(mp[0], mp[1], mp[2]), fmin3(mp[3], mp[4], mp[5]), fminf(mp[6], mp[7]));
       }
       const float mt = mp[0] * scale_log2;
       const float m_new = fmaxf(m_used, mt);
@@ -328,24 +335,26 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
       }
       // P_t over the first 32 columns of S_t's tile (this thread's S_t row
       // is already in registers).
-      float rs8[8];
+      // Eight partial row sums held as four packed pairs; the exponent
+      // arguments two columns per packed FMA.
+      const uint64_t sl2 = f32x2(scale_log2, scale_log2);
+      const uint64_t nm2 = f32x2(-m_used, -m_used);
+      uint64_t rs2[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
+      for (int e = 0; e < 4; ++e) rs2[e] = f32x2(0.f, 0.f);
       uint32_t pk[32];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
-        float p[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = ex2_approx(fmaf(x[ch * 8 + e], scale_log2, -m_used));
-          rs8[e] += p[e];
+        for (int e = 0; e < 4; ++e) {
+          const uint64_t a = ffma2(f32x2(x[ch * 8 + 2 * e], x[ch * 8 + 2 * e + 1]), sl2, nm2);
+          const float p0 = ex2_approx(f32x2_lo(a)), p1 = ex2_approx(f32x2_hi(a));
+          rs2[e] = fadd2(rs2[e], f32x2(p0, p1));
+          pk[ch * 4 + e] = pack_bf16x2(p0, p1);
         }
-        pk[ch * 4 + 0] = pack_bf16x2(p[0], p[1]);
-        pk[ch * 4 + 1] = pack_bf16x2(p[2], p[3]);
-        pk[ch * 4 + 2] = pack_bf16x2(p[4], p[5]);
-        pk[ch * 4 + 3] = pack_bf16x2(p[6], p[7]);
       }
-      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      l += ((f32x2_lo(rs2[0]) + f32x2_hi(rs2[0])) + (f32x2_lo(rs2[1]) + f32x2_hi(rs2[1]))) +
+           ((f32x2_lo(rs2[2]) + f32x2_hi(rs2[2])) + (f32x2_lo(rs2[3]) + f32x2_hi(rs2[3])));
       {
         const uint32_t pa = lane_base + C::col_s + (t & 1) * kBN;
         SPARGE_TMEM_ST_X16(pa, pk);

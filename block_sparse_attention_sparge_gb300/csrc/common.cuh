@@ -292,6 +292,18 @@ SPARGE_DEV uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Three-input fp32 max / min (one instruction on sm_100 and later).
+SPARGE_DEV float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+SPARGE_DEV float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 SPARGE_DEV float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
