@@ -53,11 +53,15 @@ constexpr unsigned kFull = 0xffffffffu;
 // ---------------------------------------------------------------- pooling
 constexpr int kPoolThreads = 256;
 
-constexpr int kPoolRows = 256;  // consecutive rows (tokens) one CTA reads
+// Consecutive rows (tokens) one CTA reads.  128-row units at four CTAs per SM
+// (64 registers a thread) keep other CTAs' loads in flight while one reduces;
+// measured at 480p: the whole mask 49.4 us against 51.1 us with 256-row
+// units at two CTAs per SM.
+constexpr int kPoolRows = 128;
 
-// Issues this thread's loads of a run of 256 rows (up to `rows` valid; d = D
+// Issues this thread's loads of a run of 128 rows (up to `rows` valid; d = D
 // bf16 values per row): 16-byte chunk t % CH of rows t / CH + RG * i
-// (i < L), all issued before any is used, so a CTA keeps 64 KB (d = 128) in
+// (i < L), all issued before any is used, so a CTA keeps 32 KB (d = 128) in
 // flight.
 template <int D>
 __device__ __forceinline__ void pool_loads(const __nv_bfloat16* __restrict__ src, int rows,
@@ -79,7 +83,7 @@ __device__ __forceinline__ void pool_loads(const __nv_bfloat16* __restrict__ src
 // i * RG / BLK of the run; the sums go to red[row group][block][feature].
 template <int D, int BLK>
 __device__ __forceinline__ void pool_accumulate(const uint4 (&v)[kPoolRows * D / 8 / kPoolThreads],
-                                                float (*red)[4][D]) {
+                                                float (*red)[kPoolRows / 64][D]) {
   constexpr int CH = D / 8;
   constexpr int RG = kPoolThreads / CH;
   constexpr int L = kPoolRows / RG;
@@ -106,14 +110,14 @@ __device__ __forceinline__ void pool_accumulate(const uint4 (&v)[kPoolRows * D /
     for (int e = 0; e < 8; ++e) red[rg][g][c * 8 + e] = acc[g][e];
 }
 
-// One CTA per unit: 256 consecutive tokens of one head, i.e. 256 / block
+// One CTA per unit: 128 consecutive tokens of one head, i.e. 128 / block
 // size blocks.  Units [0, BH*UQ) cover the Q blocks (when do_q), the rest
 // the K blocks.  The means are row-major [BH, M, d]: fp32 into qbar / kbar,
 // or, when qhi is set, as the bf16 pair hi = bf16(mean), lo = bf16(mean - hi)
 // into qhi / qlo and khi / klo (the operands of the pooled-logit MMAs,
 // hi*hi + hi*lo + lo*hi).
 template <int D>
-__global__ void __launch_bounds__(kPoolThreads) pool_kernel(
+__global__ void __launch_bounds__(kPoolThreads, 4) pool_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int BH, int N,
     int bq, int bk, int Mq, int Mk, int do_q, float* __restrict__ qbar,
     float* __restrict__ kbar, __nv_bfloat16* __restrict__ qhi, __nv_bfloat16* __restrict__ qlo,
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int CH = D / 8;
   constexpr int RG = kPoolThreads / CH;
-  __shared__ float red[RG][4][D];
+  __shared__ float red[RG][kPoolRows / 64][D];
   const int UQ = (N + kPoolRows - 1) / kPoolRows;  // units per head, either tensor
   const long long unit = blockIdx.x;
   const long long nq = do_q ? (long long)BH * UQ : 0;
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(
   }
 }
 
-// One CTA per unit of 256 tokens (units = the Q and K runs to pool).
+// One CTA per unit of 128 tokens (units = the Q and K runs to pool).
 template <int D>
 cudaError_t launch_pool_kernel(const Geom& g, const void* q, const void* k, int do_q, int do_k,
                                float* qbar, float* kbar, void* qhi, void* qlo, void* khi,
