@@ -49,7 +49,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per call of each entry point (dram__bytes_read.sum + dram__bytes_write.sum
 # summed over its kernels) from one ncu capture of the default workload (480p, 128 x 64
 # blocks, k = 5 %, p = 0) with the current kernels; reported as roofline.traffic on that workload only.
-NCU_TRAFFIC_BYTES = {("wan480", 64, 0.05, 0.0): {"bwd": 1591.5e6, "fwd": 343.8e6, "mask": 217.1e6}}
+NCU_TRAFFIC_BYTES = {("wan480", 12, 64, 0.05, 0.0): {"bwd": 1591.5e6, "fwd": 343.8e6, "mask": 217.1e6}}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -292,7 +292,13 @@ def workload_config(wl, k_frac, p, sparsity):
             "mask_rule": mask_rule(wl, k_frac, p),
             "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "block_q": wl.block_q,
             "block_kv": wl.block_kv, "k_frac": k_frac, "p": p, "sparsity": sparsity,
-            "l2": "inputs larger than L2 (Q, K, V, dO: 403 MB per step vs 129 MB L2)"}
+            "l2": l2_note(wl)}
+
+
+def l2_note(wl):
+    mb = 4 * wl.B * wl.H * wl.N * wl.d * 2 / 1e6
+    rel = "larger" if mb > 129.0 else "smaller"
+    return f"inputs {rel} than L2 (Q, K, V, dO: {mb:.0f} MB per step vs 129 MB L2)"
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -438,7 +444,7 @@ def run_ours(args, wl, k_frac, p):
                                        "frac": r["achieved"] / tc_other}
     dom = max(part_ms, key=part_ms.get)
     roofline = dict(roof[dom])
-    roofline["traffic"] = NCU_TRAFFIC_BYTES.get((wl.name, wl.block_kv, k_frac, p), {}).get(dom)
+    roofline["traffic"] = NCU_TRAFFIC_BYTES.get((wl.name, wl.H, wl.block_kv, k_frac, p), {}).get(dom)
     roofline["traffic_unit"] = "bytes per call (ncu)"
     roofline["per_launch_ms"] = part_ms[dom]
     roofline["algorithmic"] = {"fwd": "4*d per kept valid (query, key) pair",
@@ -723,6 +729,9 @@ def main(argv=None):
     ap.add_argument("--p", type=float, default=0.0, help="Top-p of the headline step (0 = off)")
     ap.add_argument("--block-kv", type=int, default=None, choices=(64, 128),
                     help="kv-block size (default: the workload's, 64)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload's shape with this many heads (e.g. a smaller case "
+                         "for profiler captures)")
     ap.add_argument("--no-hybrid", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -736,6 +745,10 @@ def main(argv=None):
     wl = synth.WORKLOADS[args.workload]
     if args.block_kv is not None:
         wl = dataclasses.replace(wl, block_kv=args.block_kv)
+    if args.heads is not None:
+        if args.heads < 1:
+            ap.error("--heads must be >= 1")
+        wl = dataclasses.replace(wl, H=args.heads)
     k_frac = wl.k_frac if args.k_frac is None else args.k_frac
     if args.impl == "reference":
         return run_reference(args, wl, k_frac, args.p)

@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(
   const int c = threadIdx.x % CH;
   float s = 0.f;
   if (r < rows) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + r * D) + c);
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + r * D) + c);
+    const uint4 a = ldg_no_l1(reinterpret_cast<const uint4*>(o + r * D) + c);
+    const uint4 b = ldg_no_l1(reinterpret_cast<const uint4*>(dout + r * D) + c);
     const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&a);
     const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll

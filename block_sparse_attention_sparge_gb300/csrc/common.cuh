@@ -101,6 +101,16 @@ SPARGE_DEV bool warp_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns = k
   return __all_sync(0xffffffffu, ok);
 }
 
+// 16-byte read-only global load that does not allocate in L1 (for data each
+// thread reads once while streaming).
+SPARGE_DEV uint4 ldg_no_l1(const uint4* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
 // ----------------------------------------------------------------- fences
 SPARGE_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

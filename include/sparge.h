@@ -184,9 +184,13 @@ int sparge_attn_fwd(const sparge_shape* shape, const void* q, const void* k, con
                     const int32_t* row_idx, const int32_t* row_cnt, float softmax_scale,
                     void* o, float* lse, int32_t* status, sparge_stream_t stream);
 
-/* Workspace bytes sparge_attn_bwd needs: fp32 D = rowsum(dO*O) per token and
- * the launch orders of kv-blocks and q-blocks (int32; lists longer than twice
- * the mean first, then index order). */
+/* Workspace bytes sparge_attn_bwd needs: fp32 D = rowsum(dO*O) per token, the
+ * work orders of the key tiles and q-blocks (int32; tiles and q-blocks with
+ * more than twice the mean work first, then index order) and four int32 work
+ * counters of the persistent gradient kernels.  Every byte is rewritten by the
+ * call itself (the counters are zeroed by its first kernel), so the buffer
+ * needs no initial contents and may be reused by the next call on the same
+ * stream. */
 int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
 
 /*
@@ -202,8 +206,19 @@ int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
  *   row_idx/cnt, col_idx/cnt : CSR and CSC lists from sparge_mask (device).
  *   dq, dk, dv       : bf16 [B,H,N,d] out.  Tokens of kv-blocks no q-block
  *                      keeps get dK = dV = 0.
- *   workspace        : device buffer of sparge_attn_bwd_workspace_bytes bytes.
- * Deterministic (no atomics).
+ *   workspace        : device buffer of sparge_attn_bwd_workspace_bytes bytes,
+ *                      16-byte aligned; two calls must not share one buffer
+ *                      concurrently (it holds their work counters).
+ *   status           : nullable; records SPARGE_ERR_TIMEOUT if a bounded wait
+ *                      of a gradient kernel runs out, SPARGE_ERR_CUDA if the
+ *                      dK/dV kernel finds its shared-memory window misaligned.
+ * The call launches three kernels: D and the work orders; dK/dV (one CTA per
+ * SM taking 128-key tiles from a work counter); dQ (one CTA per SM taking
+ * q-blocks from a second counter, started early by programmatic dependent
+ * launch; it does not read dK or dV).  Deterministic: no atomics touch the
+ * gradients, each gradient element is accumulated by one CTA in a fixed order
+ * (the counters only decide which CTA), so repeated calls give bitwise
+ * identical dQ, dK, dV.
  */
 int sparge_attn_bwd(const sparge_shape* shape, const void* q, const void* k, const void* v,
                     const void* o, const float* lse, const void* dout, const int32_t* row_idx,
