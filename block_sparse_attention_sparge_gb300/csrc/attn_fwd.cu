@@ -56,29 +56,38 @@ constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct FwdCfg {
-  static constexpr int NST = 2;                       // K/V stages
+  // K and V stages of 64 keys.  A K stage is held until S of its step, a V
+  // stage until PV.  K tiles were read by the mask's pooling just before and
+  // mostly hit L2; V tiles come from DRAM (about 2500 cycles under load), so V
+  // gets the deeper ring (measured at 480p: 0.2605 against 0.2656 ms with
+  // two stages each).
+  static constexpr int NSK = D == 128 ? 2 : 3;
+  static constexpr int NSV = D == 128 ? 3 : 4;
   static constexpr int NP = 2;                        // P phases (the S/P TMEM tiles)
   static constexpr int KCH = D / 64;                  // 128-byte chunks per row
   static constexpr uint32_t kQ = kBM * D * 2;
   static constexpr uint32_t kKV = kBN * D * 2;
   static constexpr uint32_t off_q = 0;
   static constexpr uint32_t off_k = off_q + kQ;
-  static constexpr uint32_t off_v = off_k + NST * kKV;
-  static constexpr uint32_t off_bar = off_v + NST * kKV;
+  static constexpr uint32_t off_v = off_k + NSK * kKV;
+  static constexpr uint32_t off_bar = off_v + NSV * kKV;
   // barriers
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;
-  static constexpr int B_VF = B_KF + NST;
-  static constexpr int B_KE = B_VF + NST;   // K slot free (S of its tile done)
-  static constexpr int B_VE = B_KE + NST;   // V slot free (PV of its tile done)
-  static constexpr int B_SF = B_VE + NST;
+  static constexpr int B_VF = B_KF + NSK;
+  static constexpr int B_KE = B_VF + NSV;   // K slot free (S of its tile done)
+  static constexpr int B_VE = B_KE + NSK;   // V slot free (PV of its tile done)
+  static constexpr int B_SF = B_VE + NSV;
   static constexpr int B_PF = B_SF + 2;     // count 128 (all softmax threads)
   static constexpr int B_PV = B_PF + NP;
   static constexpr int B_DRAIN = B_PV + 2;  // count 2 (both issuers)
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t off_tmem_slot = off_bar + NBAR * 8;
   static constexpr uint32_t bytes = off_tmem_slot + 16;
-  static constexpr uint32_t smem_alloc = bytes + 1024;  // slack for 1024-byte alignment
+  // The dynamic shared-memory window starts 1024-byte aligned on sm_103a
+  // (checked at kernel entry), so no alignment pad is allocated: two CTAs
+  // with three V stages then fit one SM.
+  static constexpr uint32_t smem_alloc = bytes;
   // S0 [0,64) S1 [64,128) O [128,128+D); P_t (bf16 pairs) over the first 32
   // columns of S_(t & 1).
   static constexpr uint32_t tmem_cols = 256;
@@ -96,10 +105,13 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                     int32_t* __restrict__ status) {
   using C = FwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   const uint32_t s0 = smem_u32(sm);
+  if ((s0 & 1023u) != 0u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) report_error(status, SPARGE_ERR_CUDA);
+    return;
+  }
   auto bar = [&](int i) -> uint32_t { return s0 + C::off_bar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::off_tmem_slot);
 
@@ -149,32 +161,31 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
         tma_load_3d(s0 + C::off_q + c * kBM * 128, &tmQ, bar(C::B_Q), c * 64, qb * kBM, bh);
       int issued = 0;
       for (int t = 0; t < n; ++t) {
-        const int s = t % C::NST;
-        if (t >= C::NST && !mbar_wait(bar(C::B_KE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+        const int sk = t % C::NSK, sv = t % C::NSV;
+        if (t >= C::NSK && !mbar_wait(bar(C::B_KE + sk), ((t / C::NSK) - 1) & 1, kWaitTimeoutNs)) {
           report_error(status, SPARGE_ERR_TIMEOUT);
           break;
         }
         const int rw = row_of(t);
-        mbar_arrive_expect_tx(bar(C::B_KF + s), C::kKV);
+        mbar_arrive_expect_tx(bar(C::B_KF + sk), C::kKV);
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(s0 + C::off_k + s * C::kKV + c * kBN * 128, &tmK, bar(C::B_KF + s), c * 64,
+          tma_load_3d(s0 + C::off_k + sk * C::kKV + c * kBN * 128, &tmK, bar(C::B_KF + sk), c * 64,
                       rw, bh);
-        if (t >= C::NST && !mbar_wait(bar(C::B_VE + s), ((t / C::NST) - 1) & 1, kWaitTimeoutNs)) {
+        if (t >= C::NSV && !mbar_wait(bar(C::B_VE + sv), ((t / C::NSV) - 1) & 1, kWaitTimeoutNs)) {
           report_error(status, SPARGE_ERR_TIMEOUT);
           break;
         }
-        mbar_arrive_expect_tx(bar(C::B_VF + s), C::kKV);
+        mbar_arrive_expect_tx(bar(C::B_VF + sv), C::kKV);
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(s0 + C::off_v + s * C::kKV + c * kBN * 128, &tmV, bar(C::B_VF + s), c * 64,
+          tma_load_3d(s0 + C::off_v + sv * C::kKV + c * kBN * 128, &tmV, bar(C::B_VF + sv), c * 64,
                       rw, bh);
         issued = t + 1;
       }
       // Let the last loads land before the CTA can exit (they complete on their own).
-      for (int t = max(0, issued - C::NST); t < issued; ++t) {
-        const int s = t % C::NST;
-        mbar_wait(bar(C::B_KF + s), (t / C::NST) & 1, kWaitTimeoutNs);
-        mbar_wait(bar(C::B_VF + s), (t / C::NST) & 1, kWaitTimeoutNs);
-      }
+      for (int t = max(0, issued - C::NSK); t < issued; ++t)
+        mbar_wait(bar(C::B_KF + t % C::NSK), (t / C::NSK) & 1, kWaitTimeoutNs);
+      for (int t = max(0, issued - C::NSV); t < issued; ++t)
+        mbar_wait(bar(C::B_VF + t % C::NSV), (t / C::NSV) & 1, kWaitTimeoutNs);
     }
   } else if (warp == kSWarp) {
     // ------------------------------------------------------------ S issuer
@@ -185,9 +196,9 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
       const uint64_t dk0 = sdesc_sw128(s0 + C::off_k, 16, 1024);
       bool ok = warp_wait(bar(C::B_Q), 0);
       for (int t = 0; ok && t < n; ++t) {
-        const int s = t % C::NST;
+        const int s = t % C::NSK;
         // TMEM tile t & 1 holds P(t - 2) until PV(t - 2) has completed.
-        if (!warp_wait(bar(C::B_KF + s), (t / C::NST) & 1) ||
+        if (!warp_wait(bar(C::B_KF + s), (t / C::NSK) & 1) ||
             (t >= 2 && !warp_wait(bar(C::B_PV + (t & 1)), ((t - 2) >> 1) & 1))) {
           ok = false;
           break;
@@ -215,9 +226,9 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm)
       constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
       bool ok = true;
       for (int u = 0; ok && u < n; ++u) {
-        const int su = u % C::NST;
+        const int su = u % C::NSV;
         if (!warp_wait(bar(C::B_PF + (u % C::NP)), (u / C::NP) & 1) ||
-            !warp_wait(bar(C::B_VF + su), (u / C::NST) & 1)) {
+            !warp_wait(bar(C::B_VF + su), (u / C::NSV) & 1)) {
           ok = false;
           break;
         }

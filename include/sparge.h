@@ -178,6 +178,9 @@ int sparge_mask_from_prob(const sparge_shape* shape, const float* prob, float k_
  *   row_idx, row_cnt : the CSR lists of sparge_mask (device); every index in
  *                      [0, Mk), counts in [0, Mk].
  *   o                : bf16 [B,H,N,d] out.  lse: fp32 [B,H,N] out (nullable).
+ *   status           : nullable; records SPARGE_ERR_TIMEOUT if a bounded wait
+ *                      runs out, SPARGE_ERR_CUDA if a CTA finds its
+ *                      shared-memory window misaligned.
  * A q-block with row_cnt 0 gets O = 0 and LSE = -inf.
  */
 int sparge_attn_fwd(const sparge_shape* shape, const void* q, const void* k, const void* v,
