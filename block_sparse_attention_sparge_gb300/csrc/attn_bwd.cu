@@ -12,29 +12,34 @@
 //
 // Kernels, no atomics (deterministic):
 //   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads); two extra CTAs
-//                     build the launch orders of the gradient kernels (long
-//                     work lists first, then index order: a stable partition).
-//   bwd_dkdv_kernel   one CTA per pair of adjacent 64-key kv-blocks (128 keys,
-//                     one 128-key block when block_kv = 128).  The keys are
-//                     the M = 128 rows of every MMA: S^T = K Q^T and
-//                     dP^T = V dO^T land in TMEM with a key per lane, the
-//                     compute warps turn them into P^T and dS^T in place
-//                     (bf16), and those are the A operands, read from TMEM,
-//                     of dV += P^T dO and dK += dS^T Q.  The CTA walks the
-//                     union of the two blocks' column lists; a q-block that
-//                     keeps only one of the two gets zero P and dS in the
-//                     other block's rows.  Each q-block is processed as two
-//                     halves of 64 queries, so that the S/dP tiles of one half
-//                     are computed while the compute warps work on the other
-//                     half and its gradients run.
-//   bwd_dq_kernel     one CTA per q-block; its kept kv-blocks are taken two at
-//                     a time (N = 128 keys per MMA): S = Q K^T (double-buffered
+//                     build the work orders of the gradient kernels (long
+//                     work lists first, then the rest in descending index
+//                     order) and zero their work counters.
+//   bwd_dkdv_kernel   persistent, one CTA per SM taking key tiles of 128 keys
+//                     (a pair of adjacent 64-key kv-blocks, or one 128-key
+//                     block) from a work counter.  The keys are the M = 128
+//                     rows of every MMA: S^T = K Q^T and dP^T = V dO^T land in
+//                     TMEM with a key per lane, the compute warps turn them
+//                     into P^T and dS^T in place (bf16), and those are the A
+//                     operands, read from TMEM, of dV += P^T dO and
+//                     dK += dS^T Q.  The CTA walks the union of the two
+//                     blocks' column lists; a q-block that keeps only one of
+//                     the two gets zero P and dS in the other block's rows.
+//                     Each q-block is processed as two halves of 64 queries,
+//                     so that the S/dP tiles of one half are computed while
+//                     the compute warps work on the other half and its
+//                     gradients run.
+//   bwd_dq_kernel     persistent, one CTA per SM taking q-blocks from a second
+//                     counter; a q-block's kept kv-blocks are taken two at a
+//                     time (N = 128 keys per MMA): S = Q K^T (double-buffered
 //                     in TMEM) and dP = dO V^T with Q and dO in shared memory,
 //                     dS written in place over S (bf16), dQ += dS K
-//                     accumulated in TMEM.
+//                     accumulated in TMEM.  Launched with programmatic
+//                     dependent launch beside the dK/dV grid's last tiles.
 // Every MMA is M = 128 with N >= 64 (the 64-query halves of the dK/dV kernel)
-// or N = 128.  Roles per CTA: compute warps, a TMA producer warp and two
-// MMA-issuing warps.  Every wait is bounded.
+// or N = 128, issued from a converged warp (one elected lane per MMA).  Roles
+// per CTA: compute warps, a TMA producer warp and two MMA-issuing warps.
+// Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -54,11 +59,14 @@ constexpr int kPair = 128;  // keys per gradient tile (two 64-key boxes)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- work order
-// Launch order of the gradient CTAs: the items whose work is longer than twice
-// the mean first, then the others, each group in index order (a stable
-// partition).  Long lists (attention-sink blocks that nearly every q-block
-// keeps) would otherwise run alone at the end of the grid; index order keeps
-// the CTAs of one head together, so that head's tiles are served from L2.
+// Work order of the gradient kernels: the items whose work is longer than twice
+// the mean first, in index order, then the others in descending index order.
+// Long lists (attention-sink blocks that nearly every q-block keeps) would
+// otherwise run alone at the end of the grid; index order keeps the items of
+// one head together, so that head's tiles are served from L2; descending
+// order starts the rest on the last heads, whose dO (read by the delta pass)
+// and K/V (read by the dK/dV kernel's last tiles) are still in L2 (measured
+// at 480p: 1.060 against 1.067 ms per backward).
 // One CTA of NT threads partitions the n items; work(it) gives an item's size.
 template <int NT, typename Work>
 __device__ void order_by_work(int n, Work work, int32_t* __restrict__ order) {
@@ -103,7 +111,10 @@ __device__ void order_by_work(int n, Work work, int32_t* __restrict__ order) {
   const int n_long = scan[W - 1];
   int pl = before_long;                // next long position
   int ps = n_long + lo - before_long;  // next short position
-  for (int it = lo; it < hi; ++it) order[is_long(it) ? pl++ : ps++] = it;
+  for (int it = lo; it < hi; ++it) {
+    if (is_long(it)) order[pl++] = it;
+    else order[n - 1 - (ps++ - n_long)] = it;  // short items, descending
+  }
 }
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)

@@ -189,11 +189,11 @@ int sparge_attn_fwd(const sparge_shape* shape, const void* q, const void* k, con
 
 /* Workspace bytes sparge_attn_bwd needs: fp32 D = rowsum(dO*O) per token, the
  * work orders of the key tiles and q-blocks (int32; tiles and q-blocks with
- * more than twice the mean work first, then index order) and four int32 work
- * counters of the persistent gradient kernels.  Every byte is rewritten by the
- * call itself (the counters are zeroed by its first kernel), so the buffer
- * needs no initial contents and may be reused by the next call on the same
- * stream. */
+ * more than twice the mean work first, then the rest in descending index
+ * order) and four int32 work counters of the persistent gradient kernels.
+ * Every byte is rewritten by the call itself (the counters are zeroed by its
+ * first kernel), so the buffer needs no initial contents and may be reused by
+ * the next call on the same stream. */
 int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
 
 /*
