@@ -222,8 +222,8 @@ struct DkdvCfg {
   // dV of a half proceed while dP^T and dS^T of it are still in flight.
   static constexpr int B_SSF = B_QE + NSLOT;  // 2: S^T_h in TMEM
   static constexpr int B_DPF = B_SSF + 2;     // 2: dP^T_h in TMEM
-  static constexpr int B_PPF = B_DPF + 2;     // 2, all compute threads: P^T_h written
-  static constexpr int B_DSF = B_PPF + 2;     // 2, all compute threads: dS^T_h written
+  static constexpr int B_PPF = B_DPF + 2;     // 2, half h's compute group: P^T_h written
+  static constexpr int B_DSF = B_PPF + 2;     // 2, half h's compute group: dS^T_h written
   static constexpr int B_RVF = B_DSF + 2;     // 2: dV MMAs of half h done (S^T_h region free)
   static constexpr int B_RKF = B_RVF + 2;     // 2: dK MMAs of half h done (dP^T_h region free)
   static constexpr int B_DKE = B_RKF + 2;     // all compute threads: dV, dK read out
@@ -239,10 +239,9 @@ struct DkdvCfg {
   static constexpr uint32_t smem_alloc = bytes;
   // TMEM: half h of the queries uses columns [128h, 128h + 128): S^T_h at
   // +0 (64 fp32 columns) and dP^T_h at +64.  P^T_h is written over S^T_h as
-  // bf16 pairs: the compute group holding queries NC*g .. NC*g + NC - 1 (NC
-  // = 32 with eight compute warps) writes them to columns NC*g .. NC*g +
-  // NC/2 - 1, over columns it had read; dS^T_h likewise over dP^T_h.  dV at
-  // 256, dK at 256 + 128.
+  // bf16 pairs in chunks of 32 queries: chunk c (queries 32c .. 32c + 31)
+  // goes to columns 32c .. 32c + 15, over columns it had read; dS^T_h
+  // likewise over dP^T_h.  dV at 256, dK at 256 + 128.
   static constexpr uint32_t tmem_cols = 512;
   static constexpr uint32_t col_dv = 256;
   static constexpr uint32_t col_dk = 384;
@@ -289,7 +288,7 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
     for (int i = 0; i < C::NBAR; ++i) {
       uint32_t cnt = 1;
       if (i >= C::B_QF && i < C::B_QF + C::NSLOT) cnt = 32;
-      if (i >= C::B_PPF && i < C::B_PPF + 4) cnt = 32 * R::kCompute;  // PPF, DSF
+      if (i >= C::B_PPF && i < C::B_PPF + 4) cnt = 32 * R::kCompute / 2;  // PPF, DSF: one half's group
       if (i == C::B_DKE) cnt = 32 * R::kCompute;
       if (i >= C::B_IE && i < C::B_IE + C::NRING) cnt = 2 + R::kCompute;
       if (i == C::B_DONE) cnt = 2;
@@ -525,7 +524,7 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
     // first MMAs of a tile overwrite the accumulators, after the compute
     // warps have read out the previous tile's.
     constexpr uint32_t idG = idesc_bf16(kPair, D, false, true);
-    constexpr int NC = 64 / (R::kCompute / 4);
+    constexpr int NC = 32;  // queries per P^T / dS^T chunk in TMEM
     bool ok = true;
     int t = 0, j = 0;
     for (int seq = 0;; ++seq) {
@@ -551,7 +550,7 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
           }
           tc_fence_after();
           // Queries 16kk .. 16kk + 15 of the half: the TMEM columns where the
-          // compute warp group holding them wrote their bf16 pairs.
+          // compute group wrote their chunk's bf16 pairs.
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             warp_mma_bf16_ta(tmem + C::col_dv, ap + NC * (16 * kk / NC) + (16 * kk % NC) / 2,
@@ -577,10 +576,11 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
     warp_wait(bar(C::B_DONE), 0);
   } else if (warp < R::kCompute) {
     // ---------------------------------------------------------- compute
-    // Thread = key row r (TMEM lane).  All compute warps take half 0 of an
-    // entry, then half 1; within a half, warp group g = warp / 4 takes the NC
-    // queries NC*g .. NC*g + NC - 1.
-    constexpr int NC = 64 / (R::kCompute / 4);
+    // Thread = key row r (TMEM lane).  Warp group g = warp / 4 takes query
+    // half g of every entry (all 64 queries, in two chunks of 32), so the two
+    // warps of an SM sub-partition work on different halves and their
+    // latencies overlap (measured at 480p: 1.038 against 1.059 ms per
+    // backward with both groups on the same half, 32 queries each).
     constexpr int FPW = D / (R::kCompute / 4);  // features per warp in the epilogue
     const int quarter = warp & 3, cg = warp >> 2;
     const int r = quarter * 32 + lane;
@@ -612,32 +612,37 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
         continue;
       }
       for (int e = 0; ok && e < n; ++e, ++t) {
-        for (int h = 0; h < 2; ++h) {
-          const int k = 2 * t + h, sl = k % C::NSLOT;
-          if (!warp_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1) ||
-              !warp_wait(bar(C::B_SSF + h), t & 1)) {
-            ok = false;
-            break;
-          }
-          const int flags = info[sl] >> 24;
-          const bool live = (flags & flag_bit) != 0;  // warp-uniform
-          const float* rowv = reinterpret_cast<const float*>(sm + C::off_row + sl * (2 * 64 * 4));
-          tc_fence_after();
-          const uint32_t sa = lane_base + h * 128 + NC * cg;
-          // P^T first (from S^T alone); it is the A operand of dV.
-          float p[NC];
-          uint32_t pk[NC / 2];
+        // This warp group's half of the entry: queries 64h .. 64h + 63 of the
+        // q-block, taken in two chunks of 32.
+        const int h = cg;
+        const int k = 2 * t + h, sl = k % C::NSLOT;
+        if (!warp_wait(bar(C::B_QF + sl), (k / C::NSLOT) & 1) ||
+            !warp_wait(bar(C::B_SSF + h), t & 1)) {
+          ok = false;
+          break;
+        }
+        const int flags = info[sl] >> 24;
+        const bool live = (flags & flag_bit) != 0;  // warp-uniform
+        const float* rowv = reinterpret_cast<const float*>(sm + C::off_row + sl * (2 * 64 * 4));
+        tc_fence_after();
+        // P^T first (from S^T alone); it is the A operand of dV.  Chunk c's
+        // bf16 pairs go over S^T columns 32c .. 32c + 15, which it has read.
+        float p[64];
+        const uint64_t sl2 = f32x2(scale_log2, scale_log2);
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const uint32_t sa = lane_base + h * 128 + 32 * c2;
+          uint32_t pk[16];
           if (live) {
-            uint32_t sr[NC / 16][16];
-#pragma unroll
-            for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 16 * c, sr[c]);
-#pragma unroll
-            for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(sr[c]);
+            uint32_t sr[2][16];
+            SPARGE_TMEM_LD_X16(sa, sr[0]);
+            SPARGE_TMEM_LD_X16(sa + 16, sr[1]);
+            SPARGE_TMEM_WAIT_LD16(sr[0]);
+            SPARGE_TMEM_WAIT_LD16(sr[1]);
             // Two queries per packed instruction: P^T = 2^(S^T * scale*log2e - lse*log2e).
-            const uint64_t sl2 = f32x2(scale_log2, scale_log2);
-            const ulonglong2* l4 = reinterpret_cast<const ulonglong2*>(rowv + NC * cg);
+            const ulonglong2* l4 = reinterpret_cast<const ulonglong2*>(rowv + 32 * c2);
 #pragma unroll
-            for (int g = 0; g < NC / 4; ++g) {
+            for (int g = 0; g < 8; ++g) {
               const ulonglong2 lv = l4[g];  // -lse*log2e of queries 4g .. 4g + 3
 #pragma unroll
               for (int q2 = 0; q2 < 2; ++q2) {
@@ -645,47 +650,44 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
                 const uint64_t x = ffma2(f32x2(__uint_as_float(sr[col / 16][col % 16]),
                                                __uint_as_float(sr[col / 16][col % 16 + 1])),
                                          sl2, q2 == 0 ? lv.x : lv.y);
-                p[col] = ex2_approx(f32x2_lo(x));
-                p[col + 1] = ex2_approx(f32x2_hi(x));
+                p[32 * c2 + col] = key_in ? ex2_approx(f32x2_lo(x)) : 0.f;
+                p[32 * c2 + col + 1] = key_in ? ex2_approx(f32x2_hi(x)) : 0.f;
               }
             }
-            if (!key_in) {
 #pragma unroll
-              for (int q4 = 0; q4 < NC; ++q4) p[q4] = 0.f;
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < NC / 2; ++q4) pk[q4] = pack_bf16x2(p[2 * q4], p[2 * q4 + 1]);
+            for (int q4 = 0; q4 < 16; ++q4)
+              pk[q4] = pack_bf16x2(p[32 * c2 + 2 * q4], p[32 * c2 + 2 * q4 + 1]);
           } else {
 #pragma unroll
-            for (int q4 = 0; q4 < NC; ++q4) p[q4] = 0.f;
+            for (int q4 = 0; q4 < 32; ++q4) p[32 * c2 + q4] = 0.f;
 #pragma unroll
-            for (int q4 = 0; q4 < NC / 2; ++q4) pk[q4] = 0u;
+            for (int q4 = 0; q4 < 16; ++q4) pk[q4] = 0u;
           }
-          // P^T over the first NC/2 of the NC S^T columns this thread read.
-          if constexpr (NC == 32) {
-            SPARGE_TMEM_ST_X16(sa, pk);
-          } else {
-            SPARGE_TMEM_ST_X8(sa, pk);
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(bar(C::B_PPF + h));
-          // dS^T = P^T * (dP^T - D).
-          if (!warp_wait(bar(C::B_DPF + h), t & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          SPARGE_TMEM_ST_X16(sa, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PPF + h));
+        // dS^T = P^T * (dP^T - D).
+        if (!warp_wait(bar(C::B_DPF + h), t & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const uint32_t sa = lane_base + h * 128 + 32 * c2;
+          uint32_t pk[16];
           if (live) {
-            uint32_t dr[NC / 16][16];
+            uint32_t dr[2][16];
+            SPARGE_TMEM_LD_X16(sa + 64, dr[0]);
+            SPARGE_TMEM_LD_X16(sa + 64 + 16, dr[1]);
+            SPARGE_TMEM_WAIT_LD16(dr[0]);
+            SPARGE_TMEM_WAIT_LD16(dr[1]);
+            // Two queries per packed instruction.
+            const ulonglong2* d4 = reinterpret_cast<const ulonglong2*>(rowv + 64 + 32 * c2);
 #pragma unroll
-            for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_LD_X16(sa + 64 + 16 * c, dr[c]);
-#pragma unroll
-            for (int c = 0; c < NC / 16; ++c) SPARGE_TMEM_WAIT_LD16(dr[c]);
-            // dS^T = P^T * (dP^T - D), two queries per packed instruction.
-            const ulonglong2* d4 = reinterpret_cast<const ulonglong2*>(rowv + 64 + NC * cg);
-#pragma unroll
-            for (int g = 0; g < NC / 4; ++g) {
+            for (int g = 0; g < 8; ++g) {
               const ulonglong2 dv4 = d4[g];  // -D of queries 4g .. 4g + 3
 #pragma unroll
               for (int q2 = 0; q2 < 2; ++q2) {
@@ -693,26 +695,33 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
                 const uint64_t dd = fadd2(f32x2(__uint_as_float(dr[col / 16][col % 16]),
                                                 __uint_as_float(dr[col / 16][col % 16 + 1])),
                                           q2 == 0 ? dv4.x : dv4.y);
-                const uint64_t z = fmul2(f32x2(p[col], p[col + 1]), dd);
+                const uint64_t z =
+                    fmul2(f32x2(p[32 * c2 + col], p[32 * c2 + col + 1]), dd);
                 pk[g * 2 + q2] = pack_bf16x2(f32x2_lo(z), f32x2_hi(z));
               }
             }
-          }
-          if constexpr (NC == 32) {
-            SPARGE_TMEM_ST_X16(sa + 64, pk);
           } else {
-            SPARGE_TMEM_ST_X8(sa + 64, pk);
+#pragma unroll
+            for (int q4 = 0; q4 < 16; ++q4) pk[q4] = 0u;
           }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(bar(C::B_DSF + h));
+          SPARGE_TMEM_ST_X16(sa + 64, pk);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DSF + h));
       }
       if (!ok) break;
       // Epilogue: lane r holds key r of dV and dK; warp group cg writes its
       // share of the features, then releases the accumulators to the next
-      // tile's first MMAs.
-      if (!warp_wait(bar(C::B_RKF + 1), (t - 1) & 1)) {
+      // tile's first MMAs.  Every gradient MMA of the tile is done once dK of
+      // the last entry's second half is (the pipe runs them in order).  The
+      // warps of the first half get here as soon as their own last half is
+      // done, when that barrier may still be one phase short of the last
+      // entry's previous phase (its dP^T had to wait only for the one before),
+      // so the wait takes the previous phase first: a parity wait is exact
+      // only within one phase of the barrier.
+      if ((t >= 2 && !warp_wait(bar(C::B_RKF + 1), (t - 2) & 1)) ||
+          !warp_wait(bar(C::B_RKF + 1), (t - 1) & 1)) {
         ok = false;
         break;
       }
