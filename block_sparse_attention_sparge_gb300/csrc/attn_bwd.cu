@@ -182,8 +182,9 @@ __device__ __forceinline__ void tmem_ld32u(uint32_t addr, uint32_t (&a)[16], uin
 // quarter), then a TMA producer warp, a warp issuing the S and dP MMAs and a
 // warp issuing the gradient MMAs.  The dQ kernel runs sixteen compute warps
 // (four per SM sub-partition, to hide the tensor-memory and exponential
-// latencies of its short per-thread rows); the dK/dV kernel eight, whose
-// threads carry 32 columns per query half (measured: sixteen were slower).
+// latencies of its short per-thread rows); the dK/dV kernel eight, in two
+// groups of four that take the two 64-query halves of an entry (measured:
+// sixteen warps were slower).
 template <int CW>
 struct Roles {
   static constexpr int kCompute = CW;

@@ -12,14 +12,16 @@
 // two CTAs share an SM so that one CTA's
 // latencies (barrier hand-offs, loads, its prologue and epilogue) overlap the
 // other's work.  Warp roles (224 threads):
-//   warp 4   TMA producer: Q once, then K_j / V_j into a 2-stage ring; a
-//            K slot is reloaded once S of its tile has completed, a V slot
-//            once PV of its tile has.
+//   warp 4   TMA producer: Q once, then K_j / V_j into a 2-stage K ring and
+//            a 3-stage V ring; a K slot is reloaded once S of its tile has
+//            completed, a V slot once PV of its tile has.
 //   warp 5   S issuer: S_t = Q K_t^T into a double-buffered TMEM tile
 //            (128 x 64 fp32).
 //   warp 6   PV issuer: O += P_t V_t into a TMEM accumulator (128 x d fp32),
 //            with the A operand P_t read from tensor memory.  Separate issuing
-//            warps let the S and PV MMAs of neighbouring tiles overlap.
+//            warps let the S and PV MMAs of neighbouring tiles overlap; each
+//            runs its loop as a whole warp and issues every MMA from one
+//            elected lane.
 //   warps 0-3 softmax: thread r owns query row r (= TMEM lane r).  It reads
 //            S_t, masks the ragged kv tail, keeps the running max m and sum l
 //            in base 2 and writes P_t (bf16 pairs) over the first 32 columns

@@ -44,9 +44,10 @@ cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const v
                             float* lse, int32_t* status, cudaStream_t st);
 
 // attn_bwd.cu.  Workspace: D = rowsum(dO*O) fp32 [BH, N], then the
-// launch orders of key tiles [<= BH*Mk] and q-blocks [BH*Mq] (long lists
-// first, then index order), then the work counters of the persistent
-// gradient kernels (int32 [4], zeroed by the first kernel of each call).
+// work orders of key tiles [<= BH*Mk] and q-blocks [BH*Mq] (long lists
+// first, then the rest in descending index order), then the work counters
+// of the persistent gradient kernels (int32 [4], zeroed by the first kernel
+// of each call).
 struct BwdWorkspace {
   float* delta;
   int32_t* col_order;
