@@ -10,14 +10,18 @@
 //   dV_j += P^T dO_i,  dK_j += scale * dS^T Q_i,  dQ_i += scale * dS K_j
 // with D_t = sum_c dO_tc O_tc.
 //
-// Kernels, no atomics (deterministic):
+// Kernels, deterministic (no atomics touch a gradient; each gradient element
+// is summed in a fixed order):
 //   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads); two extra CTAs
 //                     build the work orders of the gradient kernels (long
 //                     work lists first, then the rest in descending index
-//                     order) and zero their work counters.
+//                     order), cut the key tiles with far more than an SM's
+//                     share of the work into parts, and zero the counters.
 //   bwd_dkdv_kernel   persistent, one CTA per SM taking key tiles of 128 keys
 //                     (a pair of adjacent 64-key kv-blocks, or one 128-key
-//                     block) from a work counter.  The keys are the M = 128
+//                     block), or parts of them, from a work counter.  A part
+//                     covers a range of q-blocks and leaves fp32 partial dK,
+//                     dV; the last part to finish adds them in part order.  The keys are the M = 128
 //                     rows of every MMA: S^T = K Q^T and dP^T = V dO^T land in
 //                     TMEM with a key per lane, the compute warps turn them
 //                     into P^T and dS^T in place (bf16), and those are the A
@@ -59,6 +63,37 @@ constexpr int kPair = 128;  // keys per gradient tile (two 64-key boxes)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- work order
+// The planning passes below walk each thread's contiguous range in chunks of
+// kChunk items whose loads are issued together: one memory latency per chunk
+// rather than per item, so the plan stays shorter than the D pass it runs
+// beside.
+constexpr int kChunk = 8;
+
+// Exclusive prefix sum over the NT threads of a CTA; *total gets the sum.
+template <int NT, typename T>
+__device__ T block_exclusive_scan(T v, T* total) {
+  constexpr int W = NT / 32;
+  __shared__ T wsum[W];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  T incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  T before = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < W; ++i) {
+    before += i < w ? wsum[i] : 0;
+    all += wsum[i];
+  }
+  __syncthreads();  // wsum may be reused by the next call
+  *total = all;
+  return before + incl - v;
+}
+
 // Work order of the gradient kernels: the items whose work is longer than twice
 // the mean first, in index order, then the others in descending index order.
 // Long lists (attention-sink blocks that nearly every q-block keeps) would
@@ -67,84 +102,212 @@ constexpr float kLog2e = 1.4426950408889634f;
 // order starts the rest on the last heads, whose dO (read by the delta pass)
 // and K/V (read by the dK/dV kernel's last tiles) are still in L2 (measured
 // at 480p: 1.060 against 1.067 ms per backward).
-// One CTA of NT threads partitions the n items; work(it) gives an item's size.
-template <int NT, typename Work>
-__device__ void order_by_work(int n, Work work, int32_t* __restrict__ order) {
-  constexpr int W = NT / 32;
-  __shared__ long long red[W];
-  __shared__ int scan[W];
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+// One CTA of NT threads partitions the n items; work[it] is an item's size
+// (plain loads: the array may have been written by this CTA), and
+// place(pos, load(it)) records item `it` at launch position pos.
+template <int NT, typename Load, typename Place>
+__device__ void order_by_work(int n, const int32_t* work, Load load, Place place) {
+  const int tid = threadIdx.x;
   const int E = (n + NT - 1) / NT;
   const int lo = min(n, tid * E), hi = min(n, lo + E);
   long long sum = 0;
-  for (int it = lo; it < hi; ++it) sum += work(it);
+  for (int i0 = lo; i0 < hi; i0 += kChunk) {
+    int w[kChunk];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) red[w] = sum;
-  __syncthreads();
+    for (int u = 0; u < kChunk; ++u) w[u] = i0 + u < hi ? max(work[i0 + u], 0) : 0;
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) sum += w[u];
+  }
   long long total = 0;
-#pragma unroll
-  for (int i = 0; i < W; ++i) total += red[i];
+  block_exclusive_scan<NT>(sum, &total);
   // Item `it` is long when work * n > 2 * total.
-  auto is_long = [&](int it) { return (long long)work(it) * n > 2 * total; };
   int nl = 0;
-  for (int it = lo; it < hi; ++it) nl += is_long(it) ? 1 : 0;
-  int incl = nl;
+  for (int i0 = lo; i0 < hi; i0 += kChunk) {
+    int w[kChunk];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) scan[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int t = lane < W ? scan[lane] : 0;
+    for (int u = 0; u < kChunk; ++u) w[u] = i0 + u < hi ? max(work[i0 + u], 0) : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += v;
-    }
-    if (lane < W) scan[lane] = t;  // inclusive warp totals
+    for (int u = 0; u < kChunk; ++u) nl += (long long)w[u] * n > 2 * total ? 1 : 0;
   }
-  __syncthreads();
-  const int before_long = incl - nl + (w > 0 ? scan[w - 1] : 0);
-  const int n_long = scan[W - 1];
+  int n_long = 0;
+  const int before_long = block_exclusive_scan<NT>(nl, &n_long);
   int pl = before_long;                // next long position
   int ps = n_long + lo - before_long;  // next short position
-  for (int it = lo; it < hi; ++it) {
-    if (is_long(it)) order[pl++] = it;
-    else order[n - 1 - (ps++ - n_long)] = it;  // short items, descending
+  for (int i0 = lo; i0 < hi; i0 += kChunk) {
+    int w[kChunk];
+    decltype(load(0)) v[kChunk];
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      w[u] = i0 + u < hi ? max(work[i0 + u], 0) : 0;
+      v[u] = load(min(i0 + u, hi - 1));
+    }
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      if (i0 + u >= hi) break;
+      if ((long long)w[u] * n > 2 * total) place(pl++, v[u]);
+      else place(n - 1 - (ps++ - n_long), v[u]);  // short items, descending
+    }
   }
 }
 
+// The dK/dV kernel's work items in the workspace (see plan_tiles).
+struct TileItems {
+  int32_t* tile;       // key tile of each item, in tile order
+  int32_t* part;       // p | P << 8 | first partial slot << 16
+  int32_t* work;       // work of each item
+  int32_t* seq_tile;   // the items' key tiles in launch order
+  int32_t* seq_part;   // and their part words
+  int32_t* n_items;    // item count
+  int32_t* split_cnt;  // completion counters of the cut tiles
+  float* split_part;   // fp32 partial dV | dK, [slot][128 keys][2][d]
+};
+
+// Work items of the dK/dV kernel.  A key tile whose work (the summed length
+// of its column lists) is more than an SM's share of the whole, and more
+// than kMinPartWork, is cut into P <= kMaxParts parts by q-block range: part
+// p takes the q-blocks [Mq p / P, Mq (p + 1) / P) of both lists.  Each part
+// runs as its own item and leaves fp32 partial dK, dV in a workspace slot;
+// the last part to finish adds the P partials in part order and writes the
+// gradients, so the result does not depend on which CTA ran which part.
+// Without the cut, one such tile (an attention-sink block that every q-block
+// keeps) sets the kernel's length when there are few heads (measured at the
+// 480p shape with one head: 0.167 against 0.296 ms per backward).  Parts need
+// partial slots; a tile whose slots would pass max_slots stays whole.
+// Writes the items in tile order, then in launch order (long items first,
+// order_by_work), the item count and zeroed completion counters.
+constexpr int kMaxParts = 16;
+constexpr int kMinPartWork = 48;
+constexpr int kSplitSlots = 128;
+constexpr int kSplitCounters = kSplitSlots * 8;  // one per slot and compute warp
+
+template <int NT>
+__device__ void plan_tiles(const int32_t* __restrict__ col_cnt, int BH, int Mk, int Mt,
+                           int kv_per_tile, int nsm, int Mq, int max_slots, const TileItems& it) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kSplitCounters; i += NT) it.split_cnt[i] = 0;
+  const int ntiles = BH * Mt;
+  const int E = (ntiles + NT - 1) / NT;
+  const int lo = min(ntiles, tid * E), hi = min(ntiles, lo + E);
+  // Each tile's work, kept meanwhile in the launch-order tile array (written last).
+  int32_t* tile_work = it.seq_tile;
+  long long sum = 0;
+  for (int t0 = lo; t0 < hi; t0 += kChunk) {
+    int w[kChunk];
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      const int t = t0 + u;
+      int x = 0;
+      if (t < hi) {
+        const int bh = t / Mt, j0 = (t % Mt) * kv_per_tile;
+        const int32_t* c = col_cnt + (long long)bh * Mk + j0;
+        x = max(__ldg(c), 0);
+        if (kv_per_tile == 2 && j0 + 1 < Mk) x += max(__ldg(c + 1), 0);
+      }
+      w[u] = x;
+    }
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      if (t0 + u >= hi) break;
+      tile_work[t0 + u] = w[u];
+      sum += w[u];
+    }
+  }
+  long long total = 0;
+  block_exclusive_scan<NT>(sum, &total);
+  const long long L = max((long long)kMinPartWork, (total + nsm - 1) / max(nsm, 1));
+  auto parts = [&](int w) -> int {
+    return w > L ? (int)min((long long)min(kMaxParts, Mq), (w + L - 1) / L) : 1;
+  };
+  // This thread's tile work, kChunk tiles at a time.
+  auto load_work = [&](int t0, int (&w)[kChunk]) {
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) w[u] = t0 + u < hi ? tile_work[t0 + u] : 0;
+  };
+  // Slots requested, then items, each as a prefix over the tiles.
+  int req = 0;
+  for (int t0 = lo; t0 < hi; t0 += kChunk) {
+    int w[kChunk];
+    load_work(t0, w);
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      const int P = parts(w[u]);
+      req += P > 1 ? P : 0;
+    }
+  }
+  int unused = 0;
+  const int slot0 = block_exclusive_scan<NT>(req, &unused);
+  // Parts of tile t0 + u with its slots (P = 1 where they would not fit).
+  auto plan_chunk = [&](int t0, const int (&w)[kChunk], int& slot, int (&P)[kChunk],
+                        int (&base)[kChunk]) {
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      P[u] = t0 + u < hi ? parts(w[u]) : 0;
+      base[u] = 0;
+      if (P[u] > 1) {
+        const bool fits = slot + P[u] <= max_slots;
+        base[u] = slot;
+        slot += P[u];
+        if (!fits) P[u] = 1, base[u] = 0;
+      }
+    }
+  };
+  int nit = 0;
+  for (int t0 = lo, slot = slot0; t0 < hi; t0 += kChunk) {
+    int w[kChunk], P[kChunk], base[kChunk];
+    load_work(t0, w);
+    plan_chunk(t0, w, slot, P, base);
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) nit += P[u];
+  }
+  int n = 0;
+  int pos = block_exclusive_scan<NT>(nit, &n);
+  for (int t0 = lo, slot = slot0; t0 < hi; t0 += kChunk) {
+    int w[kChunk], P[kChunk], base[kChunk];
+    load_work(t0, w);
+    plan_chunk(t0, w, slot, P, base);
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      for (int p = 0; p < P[u]; ++p, ++pos) {
+        it.tile[pos] = t0 + u;
+        it.part[pos] = p | (P[u] << 8) | (base[u] << 16);
+        it.work[pos] = (w[u] + P[u] - 1) / P[u];
+      }
+    }
+  }
+  if (tid == 0) *it.n_items = n;
+  __syncthreads();  // the items are read back by other threads below
+  order_by_work<NT>(
+      n, it.work, [&](int i) { return make_int2(it.tile[i], it.part[i]); },
+      [&](int p, int2 v) {
+        it.seq_tile[p] = v.x;
+        it.seq_part[p] = v.y;
+      });
+}
+
 // ---------------------------------------------------------------- D = rowsum(dO * O)
-// The first two CTAs build the launch orders (key tiles by the summed length
-// of their column lists, q-blocks by row count) while the others stream O and
-// dO.  `kv_per_tile` is 2 when a key tile is a pair of 64-key kv-blocks.
+// The first CTA plans the dK/dV work items (key tiles by the summed length of
+// their column lists, the longest cut into parts), the second orders the
+// q-blocks by row count, while the others stream O and dO.  `kv_per_tile` is
+// 2 when a key tile is a pair of 64-key kv-blocks.  Eight CTAs per SM keep
+// enough loads in flight for the stream; at that register cap the planning
+// CTA keeps part of its state in local memory (measured at 480p: with six
+// CTAs per SM and the planner's registers the pass took 34 us instead of 30.5,
+// and the backward 5 us longer).
 template <int D>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(
+__global__ void __launch_bounds__(256, 8) bwd_delta_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, long long rows,
     float* __restrict__ delta, const int32_t* __restrict__ col_cnt, int BH, int Mk, int Mt,
-    int kv_per_tile, int32_t* __restrict__ tile_order, const int32_t* __restrict__ row_cnt,
-    int nrow, int32_t* __restrict__ row_order, int32_t* __restrict__ work) {
+    int kv_per_tile, const TileItems items, int nsm, int Mq, int max_slots,
+    const int32_t* __restrict__ row_cnt, int nrow, int32_t* __restrict__ row_order,
+    int32_t* __restrict__ work) {
   if (blockIdx.x < 2) {
     // The work counters of the persistent gradient kernels start at zero.
-    if (blockIdx.x == 0 && threadIdx.x < 4) work[threadIdx.x] = 0;
-    if (blockIdx.x == 0) {
-      auto work = [&](int it) -> long long {
-        const int bh = it / Mt, jt = it % Mt;
-        long long w = 0;
-        for (int e = 0; e < kv_per_tile; ++e) {
-          const int j = jt * kv_per_tile + e;
-          if (j < Mk) w += max(__ldg(col_cnt + (long long)bh * Mk + j), 0);
-        }
-        return w;
-      };
-      order_by_work<256>(BH * Mt, work, tile_order);
-    } else {
-      auto work = [&](int it) -> long long { return max(__ldg(row_cnt + it), 0); };
-      order_by_work<256>(nrow, work, row_order);
-    }
+    if (blockIdx.x == 0 && threadIdx.x < 2) work[threadIdx.x] = 0;
+    if (blockIdx.x == 0)
+      plan_tiles<256>(col_cnt, BH, Mk, Mt, kv_per_tile, nsm, Mq, max_slots, items);
+    else
+      order_by_work<256>(
+          nrow, row_cnt, [](int i) { return i; }, [&](int p, int i) { row_order[p] = i; });
     return;
   }
   constexpr int CH = D / 8;        // 16-byte chunks per row
@@ -195,6 +358,7 @@ struct Roles {
 };
 constexpr int kDkdvWarps = 8;
 constexpr int kDqWarps = 16;
+static_assert(kSplitCounters == kSplitSlots * kDkdvWarps, "one counter per slot and compute warp");
 
 // ---------------------------------------------------------------- dK, dV
 template <int D>
@@ -248,8 +412,9 @@ struct DkdvCfg {
   static constexpr uint32_t col_dk = 384;
 };
 
-// Persistent: one CTA per SM takes key tiles from a work counter in the
-// launch order (long column lists first).  A key tile is 128 keys: the 64-key
+// Persistent: one CTA per SM takes work items (key tiles, or parts of cut
+// tiles; plan_tiles) from a work counter in the launch order (long column
+// lists first).  A key tile is 128 keys: the 64-key
 // kv-blocks j0 = 2 * jt and j1 = 2 * jt + 1 (kv_per_tile = 2), or the one
 // 128-key block jt (kv_per_tile = 1; then both 64-row halves belong to it).
 // The entries of successive tiles share one running entry count t, which
@@ -261,7 +426,7 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const float* __restrict__ lse, const float* __restrict__ delta,
                     const int32_t* __restrict__ col_idx, const int32_t* __restrict__ col_cnt,
-                    const int32_t* __restrict__ tile_order, int ntiles, int32_t* __restrict__ work,
+                    const TileItems items, int ntiles, int32_t* __restrict__ work,
                     int N, int Mq, int Mk, int Mt, int kv_per_tile, float scale, float scale_log2,
                     __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
                     int32_t* __restrict__ status) {
@@ -284,6 +449,7 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool paired = kv_per_tile == 2;
+  const int nitems = min(max(__ldg(items.n_items), 0), ntiles + kSplitSlots);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
@@ -306,13 +472,15 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = slot[0];
 
-  // The seq-th key tile of this CTA and its entry count, as handed out by the
-  // producer through the ring (tile -1: no more work, -2: the producer gave up).
-  auto next_tile = [&](int seq, bool ok, int* n) -> int {
+  // The seq-th item of this CTA (its key tile, entry count and part word), as
+  // handed out by the producer through the ring (tile -1: no more work, -2:
+  // the producer gave up).
+  auto next_tile = [&](int seq, bool ok, int* n, int* pw) -> int {
     const int rs = seq % C::NRING;
     if (!ok || !warp_wait(bar(C::B_IF + rs), (seq / C::NRING) & 1)) return -2;
-    *n = ring[2 * rs + 1];
-    return ring[2 * rs];
+    *n = ring[4 * rs + 1];
+    *pw = ring[4 * rs + 2];
+    return ring[4 * rs];
   };
   auto release_tile = [&](int seq) { mbar_arrive(bar(C::B_IE + seq % C::NRING)); };
   struct Tile {
@@ -346,17 +514,40 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
           !mbar_wait(bar(C::B_IE + rs), ((seq / C::NRING) - 1) & 1, kWaitTimeoutNs))
         ok = false;
       ok = __all_sync(0xffffffffu, ok);
-      int it = -1;
+      int it = -1, pw = 0;
       if (ok) {
         int k = 0;
         if (lane == 0) k = atomicAdd(work, 1);
         k = __shfl_sync(0xffffffffu, k, 0);
-        it = k < ntiles ? min(max(__ldg(tile_order + k), 0), ntiles - 1) : -1;
+        if (k < nitems) {
+          it = min(max(__ldg(items.seq_tile + k), 0), ntiles - 1);
+          pw = __ldg(items.seq_part + k);
+        }
       }
       Tile x{};
       int n = 0;
       if (it >= 0) {
         x = tile_info(it);
+        const int P = (pw >> 8) & 0xff;
+        if (P > 1) {
+          // Part p of a cut tile: the entries of q-blocks [Mq p / P, Mq (p + 1) / P).
+          const int p = pw & 0xff;
+          const int qlo = (int)((long long)Mq * p / P), qhi = (int)((long long)Mq * (p + 1) / P);
+          auto lower = [&](const int32_t* l, int cnt, int v) {
+            int lo = 0, hi = cnt;
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (__ldg(l + mid) < v) lo = mid + 1; else hi = mid;
+            }
+            return lo;
+          };
+          const int a0 = lower(x.list0, x.n0, qlo), a1 = lower(x.list0, x.n0, qhi);
+          const int b0 = lower(x.list1, x.n1, qlo), b1 = lower(x.list1, x.n1, qhi);
+          x.list0 += a0;
+          x.n0 = a1 - a0;
+          x.list1 += b0;
+          x.n1 = b1 - b0;
+        }
         int common = 0;
         if (paired) {
           for (int e = lane; e < x.n0; e += 32) {
@@ -373,8 +564,9 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
         n = paired ? x.n0 + x.n1 - common : x.n0;
       }
       if (lane == 0) {
-        ring[2 * rs] = ok ? it : -2;
-        ring[2 * rs + 1] = n;
+        ring[4 * rs] = ok ? it : -2;
+        ring[4 * rs + 1] = n;
+        ring[4 * rs + 2] = pw;
         mbar_arrive(bar(C::B_IF + rs));
       }
       if (it < 0) break;
@@ -464,8 +656,8 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
     bool ok = true;
     int t = 0, j = 0;
     for (int seq = 0;; ++seq) {
-      int n = 0;
-      const int it = next_tile(seq, ok, &n);
+      int n = 0, pw = 0;
+      const int it = next_tile(seq, ok, &n, &pw);
       if (lane == 0) release_tile(seq);
       if (it < 0) {
         if (it == -2) ok = false;
@@ -529,8 +721,8 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
     bool ok = true;
     int t = 0, j = 0;
     for (int seq = 0;; ++seq) {
-      int n = 0;
-      const int it = next_tile(seq, ok, &n);
+      int n = 0, pw = 0;
+      const int it = next_tile(seq, ok, &n, &pw);
       if (lane == 0) release_tile(seq);
       if (it < 0) {
         if (it == -2) ok = false;
@@ -590,8 +782,8 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
     bool ok = true;
     int t = 0;
     for (int seq = 0;; ++seq) {
-      int n = 0;
-      const int it = next_tile(seq, ok, &n);
+      int n = 0, pw = 0;
+      const int it = next_tile(seq, ok, &n, &pw);
       __syncwarp();
       if (lane == 0) release_tile(seq);
       if (it < 0) {
@@ -601,15 +793,56 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
       const int bh = it / Mt, key0 = (it % Mt) * kPair;
       const bool key_in = key0 + r < N;
       const long long rowoff = ((long long)bh * N + key0 + r) * D;
+      // Part of a cut tile (P > 1): dV and dK of this row go to the part's
+      // fp32 slot first (dV at [0, d), dK at [d, 2d)).
+      const int P = (pw >> 8) & 0xff, slot0 = (pw >> 16) & 0xffff;
+      float* part_row =
+          items.split_part + ((long long)(slot0 + (pw & 0xff)) * kPair + r) * (2 * D);
+      // Once the part's rows are written: the warp's completion counter of the
+      // tile; the warp that completes it adds the P partials in part order
+      // (0, 1, ..., P - 1, whichever CTA ran them) and writes bf16 dV, dK.
+      auto finish_part = [&]() {
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(items.split_cnt + slot0 * kDkdvWarps + warp, 1) == P - 1;
+        if (!__shfl_sync(0xffffffffu, last, 0) || !key_in) return;
+        __threadfence();
+        const float* p0 = items.split_part + ((long long)slot0 * kPair + r) * (2 * D);
+#pragma unroll 1
+        for (int cc = cg * FPW; cc < (cg + 1) * FPW; cc += 4) {
+          float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), sk = sv;
+#pragma unroll 1
+          for (int q = 0; q < P; ++q) {
+            const float4* pr = reinterpret_cast<const float4*>(p0 + (long long)q * kPair * 2 * D);
+            const float4 v = __ldcg(pr + cc / 4), w = __ldcg(pr + (D + cc) / 4);
+            sv = q == 0 ? v : make_float4(sv.x + v.x, sv.y + v.y, sv.z + v.z, sv.w + v.w);
+            sk = q == 0 ? w : make_float4(sk.x + w.x, sk.y + w.y, sk.z + w.z, sk.w + w.w);
+          }
+          __stcs(reinterpret_cast<uint2*>(dv + rowoff + cc),
+                 make_uint2(pack_bf16x2(sv.x, sv.y), pack_bf16x2(sv.z, sv.w)));
+          __stcs(reinterpret_cast<uint2*>(dk + rowoff + cc),
+                 make_uint2(pack_bf16x2(sk.x * scale, sk.y * scale),
+                            pack_bf16x2(sk.z * scale, sk.w * scale)));
+        }
+      };
       if (n == 0) {
-        // Keys no q-block keeps: dK = dV = 0.
+        // Keys no q-block (of this part) keeps: dK = dV = 0.
         if (key_in) {
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
           for (int cc = cg * FPW; cc < (cg + 1) * FPW; cc += 8) {
-            __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc), z);
-            __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc), z);
+            if (P > 1) {
+              __stcg(reinterpret_cast<uint4*>(part_row + cc), z);
+              __stcg(reinterpret_cast<uint4*>(part_row + cc + 4), z);
+              __stcg(reinterpret_cast<uint4*>(part_row + D + cc), z);
+              __stcg(reinterpret_cast<uint4*>(part_row + D + cc + 4), z);
+            } else {
+              __stcs(reinterpret_cast<uint4*>(dv + rowoff + cc), z);
+              __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc), z);
+            }
           }
         }
+        if (P > 1) finish_part();
         continue;
       }
       for (int e = 0; ok && e < n; ++e, ++t) {
@@ -738,7 +971,15 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
           tc_fence_before();
           mbar_arrive(bar(C::B_DKE));
         }
-        if (key_in) {
+        if (key_in && P > 1) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            __stcg(reinterpret_cast<uint4*>(part_row + cc) + i,
+                   make_uint4(rv_[4 * i], rv_[4 * i + 1], rv_[4 * i + 2], rv_[4 * i + 3]));
+            __stcg(reinterpret_cast<uint4*>(part_row + D + cc) + i,
+                   make_uint4(rk_[4 * i], rk_[4 * i + 1], rk_[4 * i + 2], rk_[4 * i + 3]));
+          }
+        } else if (key_in) {
           uint4 v0, v1, k0, k1;
           v0.x = pack_bf16x2(__uint_as_float(rv_[0]), __uint_as_float(rv_[1]));
           v0.y = pack_bf16x2(__uint_as_float(rv_[2]), __uint_as_float(rv_[3]));
@@ -762,6 +1003,7 @@ __global__ void __launch_bounds__(Roles<kDkdvWarps>::kThreads, 1)
           __stcs(reinterpret_cast<uint4*>(dk + rowoff + cc + 8), k1);
         }
       }
+      if (P > 1) finish_part();
     }
     if (!ok) report_error(status, SPARGE_ERR_TIMEOUT);
   }
@@ -1239,11 +1481,20 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   const int kv_per_tile = g.bk == 64 ? 2 : 1;
   const int Mt = (g.Mk + kv_per_tile - 1) / kv_per_tile;
   const unsigned ndelta = static_cast<unsigned>((rows + RPB - 1) / RPB);
+  // Both gradient kernels are persistent: one CTA per SM (or per work item
+  // when there are fewer), taking items from their work counters.
+  int dev = 0, nsm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const TileItems items{ws.item_tile, ws.item_part, ws.item_work,   ws.seq_tile,
+                        ws.seq_part,  ws.work + 2,   ws.split_cnt, ws.split_part};
   bwd_delta_kernel<D><<<ndelta + 2, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), rows, delta,
-      col_cnt, g.BH, g.Mk, Mt, kv_per_tile, ws.col_order, row_cnt, g.BH * g.Mq, ws.row_order,
-      ws.work);
-  cudaError_t e = cudaGetLastError();
+      col_cnt, g.BH, g.Mk, Mt, kv_per_tile, items, nsm, g.Mq, kSplitSlots, row_cnt, g.BH * g.Mq,
+      ws.row_order, ws.work);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   // Q and dO in 128-row boxes for the dQ kernel, 64-row boxes (query
@@ -1257,20 +1508,14 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
     return cudaErrorInvalidValue;
   const float scale_log2 = scale * kLog2e;
 
-  // Both gradient kernels are persistent: one CTA per SM (or per work item
-  // when there are fewer), taking items from their work counters.
-  int dev = 0, nsm = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DkdvCfg<D>::smem_alloc);
   if (e != cudaSuccess) return e;
+  // Up to kSplitSlots more items than tiles (the parts of cut tiles).
   const int ntiles = g.BH * Mt;
-  bwd_dkdv_kernel<D><<<static_cast<unsigned>(max(1, min(ntiles, nsm))),
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>(max(1, min(ntiles + kSplitSlots, nsm))),
                        Roles<kDkdvWarps>::kThreads, DkdvCfg<D>::smem_alloc, st>>>(
-      tq64, tk, tv, tdo64, lse, delta, col_idx, col_cnt, ws.col_order, ntiles, ws.work + 1, g.N,
+      tq64, tk, tv, tdo64, lse, delta, col_idx, col_cnt, items, ntiles, ws.work + 1, g.N,
       g.Mq, g.Mk, Mt, kv_per_tile, scale, scale_log2, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), status);
   e = cudaGetLastError();
@@ -1315,24 +1560,46 @@ cudaError_t launch_attn_bwd(const Geom& g, const void* q, const void* k, const v
 
 namespace {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Sizes of the workspace parts, in layout order.
+constexpr int kWsParts = 10;
+void bwd_workspace_parts(const Geom& g, size_t (&sz)[kWsParts]) {
+  const int kv_per_tile = g.bk == 64 ? 2 : 1;
+  const size_t nitems = (size_t)g.BH * ((g.Mk + kv_per_tile - 1) / kv_per_tile) + kSplitSlots;
+  sz[0] = align256((size_t)g.BH * g.N * sizeof(float));            // delta
+  sz[1] = align256((size_t)g.BH * g.Mq * sizeof(int32_t));         // q-block order
+  sz[2] = align256(4 * sizeof(int32_t));                             // counters, item count
+  for (int i = 3; i < 8; ++i) sz[i] = align256(nitems * sizeof(int32_t));  // item arrays
+  sz[8] = align256(kSplitCounters * sizeof(int32_t));                // completion counters
+  sz[9] = align256((size_t)kSplitSlots * kPair * 2 * g.d * sizeof(float));  // partials
+}
 }  // namespace
 
 size_t bwd_workspace_bytes(const Geom& g) {
-  return align256((size_t)g.BH * g.N * sizeof(float)) +
-         align256((size_t)g.BH * g.Mk * sizeof(int32_t)) +
-         align256((size_t)g.BH * g.Mq * sizeof(int32_t)) + align256(4 * sizeof(int32_t));
+  size_t sz[kWsParts];
+  bwd_workspace_parts(g, sz);
+  size_t total = 0;
+  for (size_t x : sz) total += x;
+  return total;
 }
 
 BwdWorkspace bwd_workspace_layout(const Geom& g, void* base) {
-  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t sz[kWsParts];
+  bwd_workspace_parts(g, sz);
+  uint8_t* p[kWsParts];
+  p[0] = static_cast<uint8_t*>(base);
+  for (int i = 1; i < kWsParts; ++i) p[i] = p[i - 1] + sz[i - 1];
   BwdWorkspace w;
-  w.delta = reinterpret_cast<float*>(p);
-  p += align256((size_t)g.BH * g.N * sizeof(float));
-  w.col_order = reinterpret_cast<int32_t*>(p);
-  p += align256((size_t)g.BH * g.Mk * sizeof(int32_t));
-  w.row_order = reinterpret_cast<int32_t*>(p);
-  p += align256((size_t)g.BH * g.Mq * sizeof(int32_t));
-  w.work = reinterpret_cast<int32_t*>(p);
+  w.delta = reinterpret_cast<float*>(p[0]);
+  w.row_order = reinterpret_cast<int32_t*>(p[1]);
+  w.work = reinterpret_cast<int32_t*>(p[2]);
+  w.seq_tile = reinterpret_cast<int32_t*>(p[3]);
+  w.seq_part = reinterpret_cast<int32_t*>(p[4]);
+  w.item_tile = reinterpret_cast<int32_t*>(p[5]);
+  w.item_part = reinterpret_cast<int32_t*>(p[6]);
+  w.item_work = reinterpret_cast<int32_t*>(p[7]);
+  w.split_cnt = reinterpret_cast<int32_t*>(p[8]);
+  w.split_part = reinterpret_cast<float*>(p[9]);
   return w;
 }
 

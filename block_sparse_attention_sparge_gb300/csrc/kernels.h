@@ -43,16 +43,26 @@ cudaError_t launch_attn_fwd(const Geom& g, const void* q, const void* k, const v
                             const int32_t* row_idx, const int32_t* row_cnt, float scale, void* o,
                             float* lse, int32_t* status, cudaStream_t st);
 
-// attn_bwd.cu.  Workspace: D = rowsum(dO*O) fp32 [BH, N], then the
-// work orders of key tiles [<= BH*Mk] and q-blocks [BH*Mq] (long lists
-// first, then the rest in descending index order), then the work counters
-// of the persistent gradient kernels (int32 [4], zeroed by the first kernel
-// of each call).
+// attn_bwd.cu.  Workspace: D = rowsum(dO*O) fp32 [BH, N]; the q-block
+// work order [BH*Mq] (long lists first, then the rest in descending index
+// order); int32 [4]: the work counters of the persistent gradient kernels
+// and the dK/dV item count; five int32 arrays over the dK/dV items
+// [<= BH*Mt + 128]: key tile and part word in launch order, then key tile,
+// part word and work in tile order; the completion counters of cut tiles
+// (int32 [1024]) and their fp32 partial dV | dK slots [128][128][2][d].
+// The first kernel of each call rewrites the orders, items and counts and
+// zeroes the counters.
 struct BwdWorkspace {
   float* delta;
-  int32_t* col_order;
   int32_t* row_order;
   int32_t* work;
+  int32_t* seq_tile;
+  int32_t* seq_part;
+  int32_t* item_tile;
+  int32_t* item_part;
+  int32_t* item_work;
+  int32_t* split_cnt;
+  float* split_part;
 };
 size_t bwd_workspace_bytes(const Geom& g);
 BwdWorkspace bwd_workspace_layout(const Geom& g, void* base);

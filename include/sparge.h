@@ -188,12 +188,15 @@ int sparge_attn_fwd(const sparge_shape* shape, const void* q, const void* k, con
                     void* o, float* lse, int32_t* status, sparge_stream_t stream);
 
 /* Workspace bytes sparge_attn_bwd needs: fp32 D = rowsum(dO*O) per token, the
- * work orders of the key tiles and q-blocks (int32; tiles and q-blocks with
+ * work orders of the q-blocks and of the dK/dV work items (int32; items with
  * more than twice the mean work first, then the rest in descending index
- * order) and four int32 work counters of the persistent gradient kernels.
- * Every byte is rewritten by the call itself (the counters are zeroed by its
- * first kernel), so the buffer needs no initial contents and may be reused by
- * the next call on the same stream. */
+ * order), the work counters of the persistent gradient kernels, and room for
+ * cutting key tiles with far more than one SM's share of the work into at most
+ * 128 parts in all: their int32 completion counters and fp32 partial dK, dV
+ * (128 x 128 x 2 x d floats; 16 MiB at d = 128).  Every byte that is read is
+ * first written by the call itself (the counters are zeroed by its first
+ * kernel), so the buffer needs no initial contents and may be reused by the
+ * next call on the same stream. */
 int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
 
 /*
@@ -216,12 +219,15 @@ int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
  *                      of a gradient kernel runs out, SPARGE_ERR_CUDA if the
  *                      dK/dV kernel finds its shared-memory window misaligned.
  * The call launches three kernels: D and the work orders; dK/dV (one CTA per
- * SM taking 128-key tiles from a work counter); dQ (one CTA per SM taking
- * q-blocks from a second counter, started early by programmatic dependent
- * launch; it does not read dK or dV).  Deterministic: no atomics touch the
- * gradients, each gradient element is accumulated by one CTA in a fixed order
- * (the counters only decide which CTA), so repeated calls give bitwise
- * identical dQ, dK, dV.
+ * SM taking 128-key tiles from a work counter; a tile with several times an
+ * SM's share of the work, such as an attention-sink block that every q-block
+ * keeps when there are few heads, is cut into parts by q-block range whose
+ * fp32 partial dK, dV the last part to finish adds in part order); dQ (one CTA
+ * per SM taking q-blocks from a second counter, started early by programmatic
+ * dependent launch; it does not read dK or dV).  Deterministic: no atomics
+ * touch the gradients, each gradient element is accumulated in a fixed order
+ * (the counters only decide which CTA does which part), so repeated calls give
+ * bitwise identical dQ, dK, dV.
  */
 int sparge_attn_bwd(const sparge_shape* shape, const void* q, const void* k, const void* v,
                     const void* o, const float* lse, const void* dout, const int32_t* row_idx,

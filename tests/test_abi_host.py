@@ -64,8 +64,15 @@ def test_workspace_sizes(lib):
     expect = 2 * 12 * mq * 128 * 2 + 2 * 12 * mk * 128 * 2 + 12 * mq * mk * 4
     assert expect <= n.value <= expect + 5 * 256
     assert lib.sparge_attn_bwd_workspace_bytes(ctypes.byref(s), ctypes.byref(n)) == 0
-    expect = 12 * 32760 * 4 + 12 * 512 * 4 + 12 * 256 * 4
-    assert expect <= n.value <= expect + 3 * 256
+    # D per token, the q-block order, four counters, five arrays over the dK/dV
+    # items (12 heads x 256 key tiles plus 128 parts of cut tiles: tile and
+    # part word in launch order, tile, part word and work in tile order), 1024
+    # completion counters and 128 fp32 partial slots of 128 keys x (dV | dK),
+    # each of the ten regions 256-byte aligned.
+    items = 12 * 256 + 128
+    expect = (12 * 32760 * 4 + 5 * items * 4 + 12 * 256 * 4 + 4 * 4 + 1024 * 4
+              + 128 * 128 * 2 * 128 * 4)
+    assert expect <= n.value <= expect + 10 * 256
 
 
 @pytest.mark.parametrize("shape,code", [

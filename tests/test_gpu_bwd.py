@@ -142,3 +142,51 @@ def test_bwd_wan480_two_heads(wan480, k_frac, p):
             to_np(q[:, sl], np.float32), to_np(k[:, sl], np.float32), to_np(v[:, sl], np.float32),
             to_np(do[:, sl], np.float32), mask[:, sl], 128, 64, dtype=np.float32)
         _compare((dq[:, sl], dk[:, sl], dv[:, sl]), refs, f"head {h}")
+
+
+def test_bwd_cut_tiles():
+    """Key tiles whose column lists are far longer than an SM's share of the
+    work are cut into parts by q-block range, and the parts' fp32 partial
+    dK, dV are added in part order.  Two kv-blocks every q-block keeps (tile
+    0, cut into several parts), a tile kept only by the first 60 of 125
+    q-blocks (its last part has no entries: its partials are zero), a ragged
+    last q-block; both heads against the oracle, and two calls bitwise
+    equal."""
+    n = 15990
+    q, k, v, do = _rand(1, 2, n, 128, seed=29)
+    mq, mk = O.num_blocks(n, 128), O.num_blocks(n, 64)
+    mask = np.random.default_rng(29).random((1, 2, mq, mk)) < 0.04
+    mask[..., 0:2] = True
+    mask[:, :, :60, 4:6] = True
+    a = _gpu_fwd_bwd(q, k, v, do, mask)
+    b = _gpu_fwd_bwd(q, k, v, do, mask)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    refs = O.sparse_attention_blocks_bwd(
+        to_np(q, np.float32), to_np(k, np.float32), to_np(v, np.float32),
+        to_np(do, np.float32), mask, 128, 64, dtype=np.float32)
+    _compare(a, refs)
+
+
+@pytest.mark.parametrize("heads", [1, 2])
+def test_bwd_wan480_few_heads(heads):
+    """The 480p shape with one or two heads: the attention-sink tiles hold
+    several times an SM's share of the work and are cut into parts.  Every
+    head checked against the fp32 block-gather oracle; two calls bitwise
+    equal."""
+    q, k, v, do = synth.make_inputs("wan480", heads=heads)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    res = B.sparge_mask(qd, kd, 0.05, 0.0)
+    o, lse = B.sparge_attn_fwd(qd, kd, vd, res["row_idx"], res["row_cnt"], check_status=True)
+    args = (qd, kd, vd, o, lse, dod, res["row_idx"], res["row_cnt"], res["col_idx"],
+            res["col_cnt"])
+    grads = B.sparge_attn_bwd(*args, check_status=True)
+    again = B.sparge_attn_bwd(*args, check_status=True)
+    torch.cuda.synchronize()
+    for x, y in zip(grads, again):
+        assert torch.equal(x, y)
+    mask = unpack_bitmask(res["bitmask"], 512)
+    refs = O.sparse_attention_blocks_bwd(
+        to_np(q, np.float32), to_np(k, np.float32), to_np(v, np.float32),
+        to_np(do, np.float32), mask, 128, 64, dtype=np.float32)
+    _compare(grads, refs, f"{heads} heads")
