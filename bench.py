@@ -265,7 +265,7 @@ def run_reference(args, wl, k_frac, p):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(wl, k_frac, p, None),
+        "config": workload_config(wl, k_frac, p),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"per step: {nblk} q-block(s) of one head (pool, map, select, "
                                    f"fwd, bwd), NumPy fp32 block-gather oracle"},
@@ -285,14 +285,15 @@ def mask_rule(wl, k_frac, p):
     return f"hybrid Top-k + Top-p: k = {k_frac:g} (K = {kk} of {mk}), p = {p:g}"
 
 
-def workload_config(wl, k_frac, p, sparsity):
+def workload_config(wl, k_frac, p):
+    """The workload as both arms name it (the measured mask sparsity is a
+    top-level key of the library's line, so the two configs compare equal)."""
     return {"workload": (f"{wl.name}: Wan2.1-shaped attention fwd+bwd, B={wl.B}, H={wl.H}, "
                          f"N={wl.N} ({'x'.join(map(str, wl.grid))}), d={wl.d}, "
                          f"blocks {wl.block_q}x{wl.block_kv}, k={k_frac:g}, p={p:g}"),
             "mask_rule": mask_rule(wl, k_frac, p),
             "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "block_q": wl.block_q,
-            "block_kv": wl.block_kv, "k_frac": k_frac, "p": p, "sparsity": sparsity,
-            "l2": l2_note(wl)}
+            "block_kv": wl.block_kv, "k_frac": k_frac, "p": p, "l2": l2_note(wl)}
 
 
 def l2_note(wl):
@@ -613,7 +614,8 @@ def run_ours(args, wl, k_frac, p):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded smooth Gaussian Q/K fields + sinks, N(0,1) V/dO)",
-            "config": workload_config(wl, k_frac, p, sparsity),
+            "config": workload_config(wl, k_frac, p),
+            "sparsity": sparsity,
             "breakdown_ms": part_ms,
             "dense_equiv_tflops": 14.0 * d * float(Bn * H) * N * N * ws / (ms_step * 1e-3) / 1e12,
             "roofline": roofline,
