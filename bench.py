@@ -44,7 +44,7 @@ if ROOT not in sys.path:
 
 METRIC = ("sparse attn fwd+bwd ms & kept-FLOP TFLOP/s at 95% sparsity; "
           "% of BF16/HBM roofline")
-KERNELS_PER_STEP = 8  # pool, logits, select, csc, fwd, delta (+ launch orders), dkdv, dq
+KERNELS_PER_STEP = 9  # pool, logits, select, csc, fwd, plan, delta, dkdv, dq
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes per call of each entry point (dram__bytes_read.sum + dram__bytes_write.sum
 # summed over its kernels) from one ncu capture of the default workload (480p, 128 x 64
@@ -426,7 +426,7 @@ def run_ours(args, wl, k_frac, p):
         "fwd": {"kernel": "sparge_attn_fwd (attn_fwd_kernel)", "bound": "tensor",
                 "achieved": fwd_flops / (part_ms["fwd"] * 1e-3) / 1e12, "peak": tc_peak,
                 "unit": "TFLOP/s"},
-        "bwd": {"kernel": "sparge_attn_bwd (delta + dK/dV + dQ kernels)", "bound": "tensor",
+        "bwd": {"kernel": "sparge_attn_bwd (plan + delta + dK/dV + dQ kernels)", "bound": "tensor",
                 "achieved": bwd_flops / (part_ms["bwd"] * 1e-3) / 1e12, "peak": tc_peak,
                 "unit": "TFLOP/s"},
         "mask": {"kernel": "sparge_mask (pool + logits + select + csc kernels)", "bound": "hbm",

@@ -12,11 +12,12 @@
 //
 // Kernels, deterministic (no atomics touch a gradient; each gradient element
 // is summed in a fixed order):
-//   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads); two extra CTAs
-//                     build the work orders of the gradient kernels (long
+//   bwd_plan_kernel   two CTAs: the work orders of the gradient kernels (long
 //                     work lists first, then the rest in descending index
-//                     order), cut the key tiles with far more than an SM's
-//                     share of the work into parts, and zero the counters.
+//                     order), the key tiles with far more than an SM's share
+//                     of the work cut into parts, the counters zeroed.
+//   bwd_delta_kernel  D per token (HBM-bound, 16-byte loads), launched beside
+//                     the plan grid by programmatic dependent launch.
 //   bwd_dkdv_kernel   persistent, one CTA per SM taking key tiles of 128 keys
 //                     (a pair of adjacent 64-key kv-blocks, or one 128-key
 //                     block), or parts of them, from a work counter.  A part
@@ -188,9 +189,11 @@ __device__ void plan_tiles(const int32_t* __restrict__ col_cnt, int BH, int Mk, 
   const int ntiles = BH * Mt;
   const int E = (ntiles + NT - 1) / NT;
   const int lo = min(ntiles, tid * E), hi = min(ntiles, lo + E);
-  // Each tile's work, kept meanwhile in the launch-order tile array (written last).
+  // Each tile's work, kept meanwhile in the launch-order tile array (written
+  // last), and the items as they are when no tile is cut.
   int32_t* tile_work = it.seq_tile;
   long long sum = 0;
+  int wmax = 0;
   for (int t0 = lo; t0 < hi; t0 += kChunk) {
     int w[kChunk];
 #pragma unroll
@@ -209,12 +212,28 @@ __device__ void plan_tiles(const int32_t* __restrict__ col_cnt, int BH, int Mk, 
     for (int u = 0; u < kChunk; ++u) {
       if (t0 + u >= hi) break;
       tile_work[t0 + u] = w[u];
+      it.tile[t0 + u] = t0 + u;
+      it.part[t0 + u] = 1 << 8;
+      it.work[t0 + u] = w[u];
       sum += w[u];
+      wmax = max(wmax, w[u]);
     }
   }
   long long total = 0;
   block_exclusive_scan<NT>(sum, &total);
   const long long L = max((long long)kMinPartWork, (total + nsm - 1) / max(nsm, 1));
+  if (!__syncthreads_or(wmax > L)) {
+    // No tile is cut (every tile within an SM's share: the usual case with
+    // many heads); the items are the tiles.
+    if (tid == 0) *it.n_items = ntiles;
+    order_by_work<NT>(
+        ntiles, it.work, [&](int i) { return make_int2(it.tile[i], it.part[i]); },
+        [&](int p, int2 v) {
+          it.seq_tile[p] = v.x;
+          it.seq_part[p] = v.y;
+        });
+    return;
+  }
   auto parts = [&](int w) -> int {
     return w > L ? (int)min((long long)min(kMaxParts, Mq), (w + L - 1) / L) : 1;
   };
@@ -284,35 +303,44 @@ __device__ void plan_tiles(const int32_t* __restrict__ col_cnt, int BH, int Mk, 
       });
 }
 
-// ---------------------------------------------------------------- D = rowsum(dO * O)
-// The first CTA plans the dK/dV work items (key tiles by the summed length of
-// their column lists, the longest cut into parts), the second orders the
-// q-blocks by row count, while the others stream O and dO.  `kv_per_tile` is
-// 2 when a key tile is a pair of 64-key kv-blocks.  Eight CTAs per SM keep
-// enough loads in flight for the stream; at that register cap the planning
-// CTA keeps part of its state in local memory (measured at 480p: with six
-// CTAs per SM and the planner's registers the pass took 34 us instead of 30.5,
-// and the backward 5 us longer).
-template <int D>
-__global__ void __launch_bounds__(256, 8) bwd_delta_kernel(
-    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, long long rows,
-    float* __restrict__ delta, const int32_t* __restrict__ col_cnt, int BH, int Mk, int Mt,
-    int kv_per_tile, const TileItems items, int nsm, int Mq, int max_slots,
-    const int32_t* __restrict__ row_cnt, int nrow, int32_t* __restrict__ row_order,
-    int32_t* __restrict__ work) {
-  if (blockIdx.x < 2) {
+// ---------------------------------------------------------------- plan
+// Two CTAs: the first plans the dK/dV work items (key tiles by the summed
+// length of their column lists, the longest cut into parts), the second
+// orders the q-blocks by row count and zeroes the work counters.  The D pass
+// is launched as its programmatic dependent and streams beside them; its last
+// CTA waits for this grid before it exits, so the gradient kernels, launched
+// after the D pass, see the plan.  In a grid of its own the plan has the
+// registers and threads it needs without taking either from the stream
+// (measured with the plan in two extra CTAs of the D pass: 39 against 32 us
+// per pass at d = 64 and 24 heads, where 6144 key tiles are planned).
+// `kv_per_tile` is 2 when a key tile is a pair of 64-key kv-blocks.
+constexpr int kPlanThreads = 1024;
+__global__ void __launch_bounds__(kPlanThreads, 1) bwd_plan_kernel(
+    const int32_t* __restrict__ col_cnt, int BH, int Mk, int Mt, int kv_per_tile,
+    const TileItems items, int nsm, int Mq, int max_slots, const int32_t* __restrict__ row_cnt,
+    int nrow, int32_t* __restrict__ row_order, int32_t* __restrict__ work) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0) {
+    plan_tiles<kPlanThreads>(col_cnt, BH, Mk, Mt, kv_per_tile, nsm, Mq, max_slots, items);
+  } else {
     // The work counters of the persistent gradient kernels start at zero.
-    if (blockIdx.x == 0 && threadIdx.x < 2) work[threadIdx.x] = 0;
-    if (blockIdx.x == 0)
-      plan_tiles<256>(col_cnt, BH, Mk, Mt, kv_per_tile, nsm, Mq, max_slots, items);
-    else
-      order_by_work<256>(
-          nrow, row_cnt, [](int i) { return i; }, [&](int p, int i) { row_order[p] = i; });
-    return;
+    if (threadIdx.x < 2) work[threadIdx.x] = 0;
+    order_by_work<kPlanThreads>(
+        nrow, row_cnt, [](int i) { return i; }, [&](int p, int i) { row_order[p] = i; });
   }
+}
+
+// ---------------------------------------------------------------- D = rowsum(dO * O)
+// One 16-thread segment per row, 16-byte streaming loads; launched beside the
+// plan grid (above), for which its last CTA waits before exiting.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        long long rows,
+                                                        float* __restrict__ delta) {
   constexpr int CH = D / 8;        // 16-byte chunks per row
   constexpr int RPB = 256 / CH;    // rows per block pass
-  const long long r = (long long)(blockIdx.x - 2) * RPB + threadIdx.x / CH;
+  const long long r = (long long)blockIdx.x * RPB + threadIdx.x / CH;
   const int c = threadIdx.x % CH;
   float s = 0.f;
   if (r < rows) {
@@ -331,6 +359,8 @@ __global__ void __launch_bounds__(256, 8) bwd_delta_kernel(
 #pragma unroll
   for (int off = CH / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (c == 0 && r < rows) delta[r] = s;
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Loads 32 consecutive fp32 TMEM columns of this thread's lane.
@@ -1490,12 +1520,25 @@ cudaError_t launch_bwd_impl(const Geom& g, const void* q, const void* k, const v
   if (e != cudaSuccess) return e;
   const TileItems items{ws.item_tile, ws.item_part, ws.item_work,   ws.seq_tile,
                         ws.seq_part,  ws.work + 2,   ws.split_cnt, ws.split_part};
-  bwd_delta_kernel<D><<<ndelta + 2, 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), rows, delta,
-      col_cnt, g.BH, g.Mk, Mt, kv_per_tile, items, nsm, g.Mq, kSplitSlots, row_cnt, g.BH * g.Mq,
-      ws.row_order, ws.work);
+  bwd_plan_kernel<<<2, kPlanThreads, 0, st>>>(col_cnt, g.BH, g.Mk, Mt, kv_per_tile, items, nsm,
+                                               g.Mq, kSplitSlots, row_cnt, g.BH * g.Mq,
+                                               ws.row_order, ws.work);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(max(1u, ndelta));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_delta_kernel<D>, static_cast<const __nv_bfloat16*>(o),
+                           static_cast<const __nv_bfloat16*>(dout), rows, delta);
+    if (e != cudaSuccess) return e;
+  }
 
   // Q and dO in 128-row boxes for the dQ kernel, 64-row boxes (query
   // halves) for the dK/dV kernel; K and V in 64-row boxes.

@@ -218,7 +218,8 @@ int sparge_attn_bwd_workspace_bytes(const sparge_shape* shape, size_t* bytes);
  *   status           : nullable; records SPARGE_ERR_TIMEOUT if a bounded wait
  *                      of a gradient kernel runs out, SPARGE_ERR_CUDA if the
  *                      dK/dV kernel finds its shared-memory window misaligned.
- * The call launches three kernels: D and the work orders; dK/dV (one CTA per
+ * The call launches four kernels: the work orders (two CTAs); D, beside them
+ * by programmatic dependent launch; dK/dV (one CTA per
  * SM taking 128-key tiles from a work counter; a tile with several times an
  * SM's share of the work, such as an attention-sink block that every q-block
  * keeps when there are few heads, is cut into parts by q-block range whose
