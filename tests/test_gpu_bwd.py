@@ -23,13 +23,13 @@ def _rand(b, h, n, d, seed, count=4, scale=1.0):
             for _ in range(count)]
 
 
-def _gpu_fwd_bwd(q, k, v, do, mask, scale=0.0):
+def _gpu_fwd_bwd(q, k, v, do, mask, scale=0.0, bk=64):
     ridx, rcnt = mask_to_csr_tensors(mask, DEV)
     cidx, ccnt = mask_to_csc_tensors(mask, DEV)
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
-    o, lse = B.sparge_attn_fwd(qd, kd, vd, ridx, rcnt, scale, check_status=True)
+    o, lse = B.sparge_attn_fwd(qd, kd, vd, ridx, rcnt, scale, check_status=True, block_kv=bk)
     g = B.sparge_attn_bwd(qd, kd, vd, o, lse, dod, ridx, rcnt, cidx, ccnt, scale,
-                          check_status=True)
+                          check_status=True, block_kv=bk)
     torch.cuda.synchronize()
     return g
 
@@ -144,20 +144,46 @@ def test_bwd_wan480_two_heads(wan480, k_frac, p):
         _compare((dq[:, sl], dk[:, sl], dv[:, sl]), refs, f"head {h}")
 
 
-def test_bwd_cut_tiles():
+@pytest.mark.parametrize("bk", [64, 128])
+def test_bwd_cut_tiles(bk):
     """Key tiles whose column lists are far longer than an SM's share of the
     work are cut into parts by q-block range, and the parts' fp32 partial
-    dK, dV are added in part order.  Two kv-blocks every q-block keeps (tile
-    0, cut into several parts), a tile kept only by the first 60 of 125
-    q-blocks (its last part has no entries: its partials are zero), a ragged
-    last q-block; both heads against the oracle, and two calls bitwise
-    equal."""
+    dK, dV are added in part order.  The keys of the first 128-key tile are
+    kept by every q-block (cut into several parts), those of the third tile
+    only by the first 60 of 125 q-blocks (its last part has no entries: its
+    partials are zero), and the last q-block is ragged; with 64-key blocks
+    (a tile is a pair of them) and 128-key blocks; both heads against the
+    oracle, and two calls bitwise equal."""
     n = 15990
     q, k, v, do = _rand(1, 2, n, 128, seed=29)
-    mq, mk = O.num_blocks(n, 128), O.num_blocks(n, 64)
+    mq, mk = O.num_blocks(n, 128), O.num_blocks(n, bk)
+    per_tile = 128 // bk
     mask = np.random.default_rng(29).random((1, 2, mq, mk)) < 0.04
-    mask[..., 0:2] = True
-    mask[:, :, :60, 4:6] = True
+    mask[..., 0:per_tile] = True
+    mask[:, :, :60, 2 * per_tile:3 * per_tile] = True
+    mask[:, :, 60:, 2 * per_tile:3 * per_tile] = False
+    a = _gpu_fwd_bwd(q, k, v, do, mask, bk=bk)
+    b = _gpu_fwd_bwd(q, k, v, do, mask, bk=bk)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    refs = O.sparse_attention_blocks_bwd(
+        to_np(q, np.float32), to_np(k, np.float32), to_np(v, np.float32),
+        to_np(do, np.float32), mask, 128, bk, dtype=np.float32)
+    _compare(a, refs, f"block_kv {bk}")
+
+
+def test_bwd_cut_tiles_slot_limit():
+    """More tiles ask to be cut than there are partial slots: one head, the
+    first 200 of 256 kv-blocks each kept by about 60 % of the q-blocks and the
+    rest by none, so all 100 tiles of those blocks hold more than an SM's
+    share and want two parts each (200 slots of 128): the first 64 are cut,
+    the other 36 stay whole beside them.  Against the oracle; two calls
+    bitwise equal."""
+    n = 16384
+    q, k, v, do = _rand(1, 1, n, 128, seed=31)
+    mq, mk = O.num_blocks(n, 128), O.num_blocks(n, 64)
+    mask = np.zeros((1, 1, mq, mk), bool)
+    mask[..., :200] = np.random.default_rng(31).random((1, 1, mq, 200)) < 0.6
     a = _gpu_fwd_bwd(q, k, v, do, mask)
     b = _gpu_fwd_bwd(q, k, v, do, mask)
     for x, y in zip(a, b):
