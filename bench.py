@@ -49,7 +49,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per call of each entry point (dram__bytes_read.sum + dram__bytes_write.sum
 # summed over its kernels) from one ncu capture of the default workload (480p, 128 x 64
 # blocks, k = 5 %, p = 0) with the current kernels; reported as roofline.traffic on that workload only.
-NCU_TRAFFIC_BYTES = {("wan480", 12, 64, 0.05, 0.0): {"bwd": 1524.8e6, "fwd": 343.9e6, "mask": 216.5e6}}
+NCU_TRAFFIC_BYTES = {("wan480", 12, 64, 0.05, 0.0): {"bwd": 1520.7e6, "fwd": 344.0e6, "mask": 216.4e6}}
 
 
 # ----------------------------------------------------------------------------- helpers
