@@ -194,6 +194,27 @@ def test_bwd_cut_tiles_slot_limit():
     _compare(a, refs)
 
 
+def test_bwd_cut_tiles_max_parts():
+    """One 65536-token head whose first two kv-blocks every one of its 512
+    q-blocks keeps (1024 list entries against an SM's share of about 48): the
+    tile is cut into the most parts allowed, 16 ranges of 32 q-blocks, whose
+    partials are added in order.  Against the oracle; two calls bitwise
+    equal."""
+    n = 65536
+    q, k, v, do = _rand(1, 1, n, 128, seed=37)
+    mq, mk = O.num_blocks(n, 128), O.num_blocks(n, 64)
+    mask = np.random.default_rng(37).random((1, 1, mq, mk)) < 0.005
+    mask[..., 0:2] = True
+    a = _gpu_fwd_bwd(q, k, v, do, mask)
+    b = _gpu_fwd_bwd(q, k, v, do, mask)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    refs = O.sparse_attention_blocks_bwd(
+        to_np(q, np.float32), to_np(k, np.float32), to_np(v, np.float32),
+        to_np(do, np.float32), mask, 128, 64, dtype=np.float32)
+    _compare(a, refs)
+
+
 @pytest.mark.parametrize("heads", [1, 2])
 def test_bwd_wan480_few_heads(heads):
     """The 480p shape with one or two heads: the attention-sink tiles hold
